@@ -1,0 +1,183 @@
+/*
+ * libmla_prefill -- MLA (multi-head latent attention) prefill over a ragged
+ * batch and a paged K_rope cache, for one sm_103 GPU.
+ *
+ * Two stages:
+ *   mla_prefill_plan    tiles each sequence's K context into buffer rows
+ *                       (generic_flare_mla_prefill_ragged_paged_plan).
+ *   mla_prefill_ragged  ragged causal attention with a 192-wide Q head, 128
+ *                       per-head K_nope dims plus 64 K_rope dims shared by all
+ *                       heads, 128-wide V and output (flare_mla_prefill).
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer marked "device" is caller-owned device memory; the library
+ *     never allocates or frees device memory and keeps no per-call state.
+ *   - Calls are asynchronous on `stream`; none synchronises except
+ *     mla_read_device_status, which says so.  Descriptor structs are host
+ *     memory read during the call only.
+ *   - Argument errors are detected on the host before any launch and return
+ *     MLA_ERR_INVALID_ARG; nothing is enqueued in that case.  A device that is
+ *     not compute capability 10.3 gives MLA_ERR_UNSUPPORTED (there is no CPU
+ *     path).  A failed launch gives MLA_ERR_CUDA.  mla_last_error_string()
+ *     describes the last failure of the calling thread.
+ *   - `stream` is a cudaStream_t (0 = legacy default stream).
+ */
+#ifndef MLA_PREFILL_H_
+#define MLA_PREFILL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* mla_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,
+  MLA_ERR_UNSUPPORTED = 2,
+  MLA_ERR_CUDA = 3,
+} mla_status_t;
+
+typedef enum {
+  MLA_DTYPE_BF16 = 0,
+  MLA_DTYPE_FP8_E4M3 = 1, /* float8_e4m3fn: no infinities, 0x7F/0xFF are NaN */
+  MLA_DTYPE_U32 = 2,
+} mla_dtype_t;
+
+typedef enum {
+  MLA_MASK_CAUSAL = 0, /* query i of sequence b sees keys j <= cache_lens[b] + i */
+  MLA_MASK_NULL = 1,   /* every key of the sequence's context is visible */
+} mla_mask_t;
+
+typedef enum {
+  MLA_SCALE_NONE = 0,
+  MLA_SCALE_PER_TENSOR = 1, /* `scale` points at one float */
+  MLA_SCALE_PER_TOKEN = 2,  /* K_rope only: one float per pool slot, index page * P + slot */
+} mla_scale_gran_t;
+
+/* A strided view of device memory.  `data` addresses element [0, 0, ...];
+ * strides are in elements and the innermost dimension must have stride 1.
+ * fp8 tensors carry a dequantisation scale: real value = code value * scale. */
+typedef struct {
+  void* data;
+  mla_dtype_t dtype;
+  int32_t ndim;
+  int64_t shape[4];
+  int64_t stride[4];
+  const float* scale; /* device; fp8 only, else NULL */
+  mla_scale_gran_t scale_gran;
+} mla_tensor_t;
+
+/*
+ * Prefill plan (generic_flare_mla_prefill_ragged_paged_plan: summary; Args:
+ * input_row_offsets, buffer_token_size, buffer_row_offsets, cache_offsets,
+ * buffer_lengths).
+ *
+ * Sequence b has n_b = input_row_offsets[b+1] - input_row_offsets[b] new tokens
+ * and cache_lens[b] previously cached tokens; its K context holds
+ * L_b = cache_lens[b] + n_b tokens.  The contexts are packed in batch order
+ * (G_b = L_0 + ... + L_{b-1}, S = G_batch) and cut into buffer rows of
+ * T = buffer_token_size tokens; R = ceil(S / T) rows are used.  For every row
+ * r < max_buffer_rows:
+ *   buffer_row_offsets[r*(batch+1) + b] = clamp(G_b - r*T, 0, T)   (b = 0..batch)
+ *   cache_offsets[r*batch + b]          = clamp(r*T - G_b, 0, L_b)
+ *   buffer_lengths[r]                   = min(T, S - r*T) if r < R, else -1
+ * so row r holds tokens [cache_offsets[r,b], cache_offsets[r,b] + len) of
+ * sequence b at positions [buffer_row_offsets[r,b], buffer_row_offsets[r,b+1]).
+ *
+ *   input_row_offsets  device uint32 [batch+1], non-decreasing, first entry 0
+ *   cache_lens         device uint32 [batch], prior (cached) length per sequence
+ *   batch              1 .. 16384
+ *   buffer_token_size  T >= 1
+ *   max_buffer_rows    rows the three outputs have room for (may be 0)
+ *   buffer_row_offsets device uint32 [max_buffer_rows, batch+1] (written)
+ *   cache_offsets      device uint32 [max_buffer_rows, batch]   (written)
+ *   buffer_lengths     device int32  [max_buffer_rows]          (written)
+ *   num_rows           device uint32 [1] or NULL: receives R; rows past
+ *                      max_buffer_rows are not written.  If S does not fit in
+ *                      32 bits it receives 0xFFFFFFFF and the outputs are
+ *                      unspecified.
+ * One kernel launch, no host synchronisation.
+ */
+mla_status_t mla_prefill_plan(const uint32_t* input_row_offsets, const uint32_t* cache_lens,
+                              uint32_t batch, uint32_t buffer_token_size,
+                              uint32_t max_buffer_rows, uint32_t* buffer_row_offsets,
+                              uint32_t* cache_offsets, int32_t* buffer_lengths,
+                              uint32_t* num_rows, mla_stream_t stream);
+
+/* Rows needed for a K total of at most `total_k_upper_bound` tokens:
+ * ceil(total_k_upper_bound / buffer_token_size); 0 if buffer_token_size is 0. */
+uint32_t mla_prefill_plan_max_rows(uint64_t total_k_upper_bound, uint32_t buffer_token_size);
+
+/* Bytes of device workspace mla_prefill_ragged needs for `batch` sequences. */
+size_t mla_prefill_ragged_workspace_size(uint32_t batch);
+
+/*
+ * Ragged MLA prefill attention (flare_mla_prefill: description; Args: output,
+ * q, k, v, k_rope, mask_functor, valid_length, scale; the k_rope_scales
+ * overload for fp8 K_rope).
+ *
+ * For sequence b (B = page_table->shape[0]) with n_b new tokens at rows
+ * row_offsets[b] .. row_offsets[b+1]-1 of q/out, prior length p_b =
+ * cache_lens[b] and context L_b = p_b + n_b whose K/V rows are
+ * G_b .. G_b + L_b - 1 of k_nope/v (G_b = L_0 + ... + L_{b-1}), every head h
+ * and query i < n_b:
+ *   K[j]   = [ k_nope[G_b + j, h, 0:128] , k_rope(b, j)[0:64] ]
+ *   k_rope(b, j) = k_rope_pages[page_table[b, j / P], j % P, 0:64]
+ *   s_j    = scale * dot(q[row_offsets[b] + i, h, 0:192], K[j])
+ *   out[row_offsets[b] + i, h, :] = sum_j softmax(s)_j * v[G_b + j, h, :]
+ * over the keys the mask leaves visible (causal: j <= p_b + i; null: j < L_b).
+ *
+ *   out          device bf16 [Tq, H, 128]                       (written)
+ *   q            device [Tq, H, 192], bf16 or fp8 (per-tensor scale);
+ *                dims 0..127 pair with k_nope, 128..191 with K_rope
+ *   k_nope, v    device [Sk, H, 128], same dtype as q (fp8: per-tensor scale),
+ *                Sk >= sum of L_b
+ *   k_rope_pages device [num_pages, P, 64]; stride[1] (token stride) may exceed
+ *                64, e.g. the rope tail of a wider latent row.  bf16 with bf16
+ *                q; fp8 (per-token scale) with fp8 q.
+ *   page_table   device uint32 [B, max_pages]; entries must be < num_pages for
+ *                every page a context touches
+ *   row_offsets  device uint32 [B+1], non-decreasing, first entry 0, last = Tq
+ *   cache_lens   device uint32 [B]
+ *   scale        softmax scale applied to q.k (typically 1/sqrt(192))
+ *   workspace    device, >= mla_prefill_ragged_workspace_size(B) bytes,
+ *                256-byte aligned; overwritten by every call, so concurrent
+ *                calls need distinct workspaces.  Its first uint32 is the
+ *                device status word (0 = ok; see mla_read_device_status).
+ * Shapes, dtypes, strides, alignment and 32-bit index limits are checked on the
+ * host.  Offsets and page ids live on the device: an out-of-range page id or
+ * page-table column makes the kernel skip that load and set a status bit
+ * (MLA_DEVICE_STATUS_*) instead of faulting.
+ * Two launches (a one-CTA scheduler, then the persistent attention kernel);
+ * no host synchronisation; usable under stream capture.
+ */
+mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_tensor_t* q,
+                                const mla_tensor_t* k_nope, const mla_tensor_t* v,
+                                const mla_tensor_t* k_rope_pages, const mla_tensor_t* page_table,
+                                const uint32_t* row_offsets, const uint32_t* cache_lens,
+                                float scale, mla_mask_t mask, void* workspace,
+                                size_t workspace_bytes, mla_stream_t stream);
+
+/* Device status bits written into the workspace's first uint32. */
+#define MLA_DEVICE_STATUS_BAD_PAGE 0x1u    /* page id >= num_pages */
+#define MLA_DEVICE_STATUS_BAD_COLUMN 0x2u  /* context needs more pages than max_pages */
+#define MLA_DEVICE_STATUS_BAD_OFFSETS 0x4u /* row offsets decrease or exceed Tq/Sk */
+#define MLA_DEVICE_STATUS_TIMEOUT 0x8u     /* a pipeline wait gave up (kernel bug) */
+
+/* Synchronising helper: waits for `stream`, then copies the status word of
+ * `workspace` to *status_out. */
+mla_status_t mla_read_device_status(const void* workspace, uint32_t* status_out,
+                                    mla_stream_t stream);
+
+/* Text for the last error returned to the calling thread (never NULL). */
+const char* mla_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_PREFILL_H_ */

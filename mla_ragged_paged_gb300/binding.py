@@ -1,0 +1,168 @@
+"""ctypes binding for libmla_prefill (argument marshalling only).
+
+Every computation happens in the CUDA library; this module turns torch CUDA
+tensors into the C descriptors of include/mla_prefill.h and calls the entry
+points on torch's current stream.  There is no fallback: if the library is
+missing or the device is unsupported the call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+from .buildlib import LIB_PATH
+
+MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, 1, 2, 3
+MLA_DTYPE_BF16, MLA_DTYPE_FP8_E4M3, MLA_DTYPE_U32 = 0, 1, 2
+MLA_MASK_CAUSAL, MLA_MASK_NULL = 0, 1
+MLA_SCALE_NONE, MLA_SCALE_PER_TENSOR, MLA_SCALE_PER_TOKEN = 0, 1, 2
+STATUS_BITS = {0x1: "BAD_PAGE", 0x2: "BAD_COLUMN", 0x4: "BAD_OFFSETS", 0x8: "TIMEOUT"}
+
+# Names exported by the C ABI (kept in step with include/mla_prefill.h).
+EXPORTS = ["mla_prefill_plan", "mla_prefill_plan_max_rows", "mla_prefill_ragged_workspace_size",
+           "mla_prefill_ragged", "mla_read_device_status", "mla_last_error_string"]
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"libmla_prefill status {status}: {message}")
+        self.status = status
+
+
+class MlaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4),
+                ("scale", ctypes.c_void_p), ("scale_gran", ctypes.c_int)]
+
+
+_lib = None
+
+
+def load(path=LIB_PATH):
+    """Load the library (built beforehand by mla_ragged_paged_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise MlaError(-1, f"{path} is missing; build it with mla_ragged_paged_gb300.build()")
+    lib = ctypes.CDLL(path)
+    vp, u32, i32 = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int32
+    lib.mla_prefill_plan.argtypes = [vp, vp, u32, u32, u32, vp, vp, vp, vp, vp]
+    lib.mla_prefill_plan.restype = ctypes.c_int
+    lib.mla_prefill_plan_max_rows.argtypes = [ctypes.c_uint64, u32]
+    lib.mla_prefill_plan_max_rows.restype = u32
+    lib.mla_prefill_ragged_workspace_size.argtypes = [u32]
+    lib.mla_prefill_ragged_workspace_size.restype = ctypes.c_size_t
+    pt = ctypes.POINTER(MlaTensor)
+    lib.mla_prefill_ragged.argtypes = [pt, pt, pt, pt, pt, pt, vp, vp, ctypes.c_float, ctypes.c_int,
+                                       vp, ctypes.c_size_t, vp]
+    lib.mla_prefill_ragged.restype = ctypes.c_int
+    lib.mla_read_device_status.argtypes = [vp, ctypes.POINTER(u32), vp]
+    lib.mla_read_device_status.restype = ctypes.c_int
+    lib.mla_last_error_string.argtypes = []
+    lib.mla_last_error_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status):
+    if status != MLA_OK:
+        raise MlaError(status, load().mla_last_error_string().decode())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def describe(t, dtype, scale=None, scale_gran=MLA_SCALE_NONE):
+    """MlaTensor for a torch tensor (element strides, up to 4 dims)."""
+    d = MlaTensor()
+    d.data = t.data_ptr()
+    d.dtype = dtype
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    d.scale = None if scale is None else scale.data_ptr()
+    d.scale_gran = scale_gran
+    return d
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return MLA_DTYPE_BF16
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return MLA_DTYPE_FP8_E4M3
+    if t.dtype in (torch.int32,) or str(t.dtype) == "torch.uint32":
+        return MLA_DTYPE_U32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def plan_max_rows(total_k_upper_bound, buffer_token_size):
+    return int(load().mla_prefill_plan_max_rows(int(total_k_upper_bound), int(buffer_token_size)))
+
+
+def plan(input_row_offsets, cache_lens, buffer_token_size, max_rows, stream=None, out=None):
+    """mla_prefill_plan on device int32/uint32 tensors.  Returns
+    (buffer_row_offsets [R_max,B+1], cache_offsets [R_max,B], buffer_lengths [R_max],
+    num_rows [1]) as int32 device tensors holding the uint32 / int32 values."""
+    lib = load()
+    B = input_row_offsets.numel() - 1
+    dev = input_row_offsets.device
+    if out is None:
+        bro = torch.empty((max_rows, B + 1), dtype=torch.int32, device=dev)
+        co = torch.empty((max_rows, B), dtype=torch.int32, device=dev)
+        blen = torch.empty((max_rows,), dtype=torch.int32, device=dev)
+        nrows = torch.empty((1,), dtype=torch.int32, device=dev)
+    else:
+        bro, co, blen, nrows = out
+    _check(lib.mla_prefill_plan(_ptr(input_row_offsets), _ptr(cache_lens), B, int(buffer_token_size),
+                                int(max_rows), _ptr(bro), _ptr(co), _ptr(blen), _ptr(nrows),
+                                _stream(stream)))
+    return bro, co, blen, nrows
+
+
+def workspace_size(batch):
+    return int(load().mla_prefill_ragged_workspace_size(int(batch)))
+
+
+def alloc_workspace(batch, device="cuda"):
+    return torch.zeros(workspace_size(batch), dtype=torch.uint8, device=device)
+
+
+def prefill_ragged(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens, scale,
+                   mask=MLA_MASK_CAUSAL, workspace=None, q_scale=None, k_scale=None, v_scale=None,
+                   k_rope_scales=None, stream=None):
+    """mla_prefill_ragged.  fp8 inputs take per-tensor scale tensors (1 float on
+    the device) and a per-token K_rope scale tensor [num_pages, P]."""
+    lib = load()
+    B = page_table.shape[0]
+    if workspace is None:
+        workspace = alloc_workspace(B, q.device)
+    fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
+    gran_t = MLA_SCALE_PER_TENSOR if fp8 else MLA_SCALE_NONE
+    d_out = describe(out, MLA_DTYPE_BF16)
+    d_q = describe(q, _dtype_code(q), q_scale if fp8 else None, gran_t)
+    d_k = describe(k_nope, _dtype_code(k_nope), k_scale if fp8 else None, gran_t)
+    d_v = describe(v, _dtype_code(v), v_scale if fp8 else None, gran_t)
+    d_r = describe(k_rope_pages, _dtype_code(k_rope_pages), k_rope_scales if fp8 else None,
+                   MLA_SCALE_PER_TOKEN if fp8 else MLA_SCALE_NONE)
+    d_pt = describe(page_table, MLA_DTYPE_U32)
+    _check(lib.mla_prefill_ragged(ctypes.byref(d_out), ctypes.byref(d_q), ctypes.byref(d_k),
+                                  ctypes.byref(d_v), ctypes.byref(d_r), ctypes.byref(d_pt),
+                                  _ptr(row_offsets), _ptr(cache_lens), float(scale), int(mask),
+                                  _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def device_status(workspace, stream=None):
+    """Synchronising read of the workspace status word (0 = ok)."""
+    val = ctypes.c_uint32(0)
+    _check(load().mla_read_device_status(_ptr(workspace), ctypes.byref(val), _stream(stream)))
+    return int(val.value)

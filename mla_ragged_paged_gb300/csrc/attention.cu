@@ -1,0 +1,869 @@
+// Ragged causal MLA prefill attention for sm_103a (flare_mla_prefill:
+// description and Args).
+//
+// Per work item (sequence b, head h, block of 256 query rows split into two
+// 128-row tiles Q0/Q1) one CTA streams the sequence's K context in 128-key
+// tiles:
+//   S_q  = Q_q . [K_nope | K_rope]^T         (UMMA, K = 192, fp32 in TMEM)
+//   P_q  = exp2(S_q * scale * log2(e) - m)   (one thread per query row)
+//   O_q += P_q . V                           (UMMA, A = P read from TMEM)
+// The two Q tiles ping-pong so one tile's softmax overlaps the other tile's
+// GEMMs.  K_rope (64 dims shared by every head) is fetched from the paged
+// pool through the page table, one TMA box per page segment.
+//
+// Warp roles (384 threads):
+//   warp 0      producer: work-item fetch (atomic counter), TMA loads
+//   warp 1      UMMA issuer (one thread) and tensor-memory owner
+//   warps 2-3   idle
+//   warps 4-7   softmax + epilogue for Q0 (TMEM lanes 0..127)
+//   warps 8-11  softmax + epilogue for Q1
+// Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,384)
+// O1 [384,512); P_q is written as packed bf16 over the first 64 columns of S_q.
+// Shared memory: Q0/Q1 (3 x 16 KB each, 128B-swizzled K-major) and a ring of
+// eight 16 KB chunks carrying, per KV tile, K_nope[0:64], K_nope[64:128],
+// K_rope, V[:, 0:64], V[:, 64:128].
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "host_common.h"
+#include "sm103.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kBM = 128;          // query rows per tile
+constexpr int kBN = 128;          // keys per KV tile
+constexpr int kQRows = 2 * kBM;   // query rows per work item
+constexpr int kChunk = 16384;     // 128 rows x 128 bytes
+constexpr int kRing = 8;
+constexpr int kChunksPerTile = 5;
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+// Tensor-memory column of S_q / O_q.
+__device__ __forceinline__ uint32_t col_s(int q) { return q ? 128u : 0u; }
+__device__ __forceinline__ uint32_t col_o(int q) { return q ? 384u : 256u; }
+constexpr uint32_t kMaxBatch = 4096;
+constexpr uint64_t kL2GroupBytes = 32ull << 20;  // K/V bytes a head group should keep in L2
+constexpr float kRescaleThreshold = 8.0f;         // log2 units
+
+struct WsHeader {
+  uint32_t status;
+  uint32_t counter;
+  uint32_t total_items;
+  uint32_t num_seqs;
+  uint32_t pad[60];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header");
+
+// One sequence, in scheduling order.
+struct SeqRec {
+  uint32_t q_start, n, prior, kv_start, b, nqb, group, item_start;
+};
+
+struct ItemInfo {
+  int32_t valid, b, h, q_row0, i0, n, prior, L, kv_row0, n0, n1, nkv0, nkv1, pad[3];
+};
+
+struct AttnParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_rope;
+  uint16_t* out;
+  long long out_tok, out_head;
+  const uint32_t* page_table;
+  long long pt_stride;
+  const uint8_t* rope_base;
+  long long rope_tok_bytes, rope_page_bytes;
+  uint32_t max_pages, num_pages, page_size, rope_box, rope_manual;
+  uint32_t H, causal;
+  float sl2;
+  uint8_t* ws;
+};
+
+struct __align__(1024) Smem {
+  uint8_t q[2][3][kChunk];
+  uint8_t ring[kRing][kChunk];
+  uint64_t item_full[2], item_empty[2];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t kv_full[kRing], kv_empty[kRing];
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t drain;
+  ItemInfo items[2];
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+  return true;
+}
+
+// ------------------------------------------------------------ scheduler
+// One CTA: validates the ragged offsets, orders sequences longest context
+// first, picks a head-group size per sequence so a group's K/V fits in L2,
+// and writes the per-sequence records the attention kernel decodes work
+// items from.  Work item order inside a sequence: head group, then query
+// block from last (most keys) to first, then head.
+constexpr int kSchedThreads = 1024;
+
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* warp_tot, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = x;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t t = warp_tot[lane];
+    uint32_t ti = t;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      uint32_t y = __shfl_up_sync(0xffffffffu, ti, d);
+      if (lane >= d) ti += y;
+    }
+    warp_tot[lane] = ti - t;
+    if (lane == 31) *total = ti;
+  }
+  __syncthreads();
+  uint32_t r = warp_tot[warp] + incl - x;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kSchedThreads, 1)
+schedule_kernel(const uint32_t* __restrict__ ro, const uint32_t* __restrict__ cl, uint32_t B,
+                uint32_t H, uint32_t Tq, uint32_t Sk, uint32_t P, uint32_t max_pages,
+                uint32_t kv_bytes_per_key_head, uint8_t* __restrict__ ws) {
+  extern __shared__ uint32_t sm[];
+  uint32_t* kv_start = sm;           // [B]
+  uint32_t* key = sm + B;            // [B]  context length (0 = no work)
+  uint32_t* order = sm + 2 * B;      // [B]  scheduling position -> sequence
+  __shared__ uint32_t warp_tot[32];
+  __shared__ uint32_t total_s;
+  __shared__ uint32_t status_s;
+  const int tid = threadIdx.x;
+  if (tid == 0) status_s = 0;
+  __syncthreads();
+
+  // Context starts: chunked exclusive scan of L_b (64-bit guarded).
+  const uint32_t per = (B + kSchedThreads - 1) / kSchedThreads;
+  const uint32_t b0 = min(B, tid * per), b1 = min(B, b0 + per);
+  uint64_t local = 0;
+  uint32_t bad = 0;
+  for (uint32_t b = b0; b < b1; ++b) {
+    const uint32_t lo = ro[b], hi = ro[b + 1];
+    if (hi < lo || hi > Tq) bad |= MLA_DEVICE_STATUS_BAD_OFFSETS;
+    local += static_cast<uint64_t>(cl[b]) + (hi >= lo ? hi - lo : 0u);
+  }
+  const uint32_t local32 = local > 0x7FFFFFFFull ? 0x7FFFFFFFu : static_cast<uint32_t>(local);
+  uint32_t run = block_excl_scan(local32, warp_tot, &total_s);
+  for (uint32_t b = b0; b < b1; ++b) {
+    const uint32_t lo = ro[b], hi = ro[b + 1];
+    const uint32_t n = hi >= lo ? hi - lo : 0u;
+    const uint64_t L = static_cast<uint64_t>(cl[b]) + n;
+    uint32_t k = static_cast<uint32_t>(L);
+    if (hi < lo || hi > Tq || static_cast<uint64_t>(run) + L > Sk) {
+      bad |= MLA_DEVICE_STATUS_BAD_OFFSETS;
+      k = 0;
+    } else if ((L + P - 1) / P > max_pages) {
+      bad |= MLA_DEVICE_STATUS_BAD_COLUMN;
+      k = 0;
+    }
+    if (n == 0) k = 0;
+    kv_start[b] = run;
+    key[b] = k;
+    run += static_cast<uint32_t>(min(L, static_cast<uint64_t>(0x7FFFFFFFu)));
+  }
+  if (bad) atomicOr(&status_s, bad);
+  __syncthreads();
+
+  // Longest context first (stable); identity order for very large batches.
+  for (uint32_t b = tid; b < B; b += kSchedThreads) {
+    uint32_t rank = b;
+    if (B <= 2048) {
+      rank = 0;
+      const uint32_t kb = key[b];
+      for (uint32_t c = 0; c < B; ++c) {
+        const uint32_t kc = key[c];
+        rank += (kc > kb) || (kc == kb && c < b);
+      }
+    }
+    order[rank] = b;
+  }
+  __syncthreads();
+
+  // Item counts in scheduling order, then their exclusive scan.
+  uint32_t cnt_local = 0;
+  for (uint32_t s = b0; s < b1; ++s) {
+    const uint32_t b = order[s];
+    const uint32_t n = key[b] ? ro[b + 1] - ro[b] : 0u;
+    cnt_local += ((n + kQRows - 1) / kQRows) * H;
+  }
+  uint32_t item = block_excl_scan(cnt_local, warp_tot, &total_s);
+  SeqRec* recs = reinterpret_cast<SeqRec*>(ws + sizeof(WsHeader));
+  for (uint32_t s = b0; s < b1; ++s) {
+    const uint32_t b = order[s];
+    SeqRec r;
+    r.b = b;
+    r.q_start = ro[b];
+    r.n = key[b] ? ro[b + 1] - ro[b] : 0u;
+    r.prior = cl[b];
+    r.kv_start = kv_start[b];
+    r.nqb = (r.n + kQRows - 1) / kQRows;
+    const uint64_t head_bytes = static_cast<uint64_t>(key[b]) * kv_bytes_per_key_head;
+    uint64_t g = head_bytes ? kL2GroupBytes / head_bytes : H;
+    if (g > H) g = H;
+    if (g < 1) g = 1;
+    r.group = static_cast<uint32_t>(g);
+    r.item_start = item;
+    recs[s] = r;
+    item += r.nqb * H;
+  }
+  if (tid == 0) {
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    hdr->status = status_s;
+    hdr->counter = 0;
+    hdr->total_items = total_s;
+    hdr->num_seqs = B;
+  }
+}
+
+// ------------------------------------------------------------ attention
+__device__ __forceinline__ ItemInfo decode_item(uint32_t t, const WsHeader* hdr, const SeqRec* recs,
+                                                uint32_t H, uint32_t causal) {
+  ItemInfo it = {};
+  const uint32_t total = hdr->total_items;
+  if (t >= total) return it;
+  // Last sequence whose first item is <= t (sequences without items share
+  // their start with the next one, so they are never selected).
+  uint32_t lo = 0, hi = hdr->num_seqs;
+  while (hi - lo > 1) {
+    const uint32_t mid = (lo + hi) >> 1;
+    if (recs[mid].item_start <= t) lo = mid; else hi = mid;
+  }
+  const SeqRec r = recs[lo];
+  const uint32_t u = t - r.item_start;
+  const uint32_t G = r.group;
+  const uint32_t g = u / (r.nqb * G);
+  const uint32_t rem = u - g * r.nqb * G;
+  const uint32_t Gg = min(G, H - g * G);
+  const uint32_t qrev = rem / Gg;
+  const uint32_t hh = rem - qrev * Gg;
+  const int qblk = static_cast<int>(r.nqb - 1 - qrev);
+  it.valid = 1;
+  it.b = static_cast<int>(r.b);
+  it.h = static_cast<int>(g * G + hh);
+  it.n = static_cast<int>(r.n);
+  it.prior = static_cast<int>(r.prior);
+  it.L = it.n + it.prior;
+  it.i0 = qblk * kQRows;
+  it.q_row0 = static_cast<int>(r.q_start) + it.i0;
+  it.kv_row0 = static_cast<int>(r.kv_start);
+  it.n0 = min(kBM, it.n - it.i0);
+  it.n1 = max(0, min(kBM, it.n - it.i0 - kBM));
+  const int all_tiles = (it.L + kBN - 1) / kBN;
+  it.nkv0 = causal ? (it.prior + it.i0 + it.n0 - 1) / kBN + 1 : all_tiles;
+  it.nkv1 = it.n1 > 0 ? (causal ? (it.prior + it.i0 + kBM + it.n1 - 1) / kBN + 1 : all_tiles) : 0;
+  return it;
+}
+
+struct Ring {
+  uint32_t full, empty, data;  // shared addresses of kv_full[0], kv_empty[0], ring[0]
+  __device__ __forceinline__ uint32_t slot(uint32_t pos) const { return pos % kRing; }
+  __device__ __forceinline__ uint32_t phase(uint32_t pos) const { return (pos / kRing) & 1u; }
+  __device__ __forceinline__ uint32_t full_bar(uint32_t pos) const { return full + 8u * slot(pos); }
+  __device__ __forceinline__ uint32_t empty_bar(uint32_t pos) const { return empty + 8u * slot(pos); }
+  __device__ __forceinline__ uint32_t buf(uint32_t pos) const { return data + kChunk * slot(pos); }
+};
+
+__device__ void producer_warp(Smem& s, const AttnParams& p, int lane, volatile uint32_t* abort) {
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
+  const SeqRec* recs = reinterpret_cast<const SeqRec*>(p.ws + sizeof(WsHeader));
+  const Ring ring{smem_u32(&s.kv_full[0]), smem_u32(&s.kv_empty[0]), smem_u32(&s.ring[0][0])};
+  uint32_t pos = 0, item_k = 0, q_uses[2] = {0, 0};
+  uint32_t status = 0;
+  bool alive = true;
+
+  auto acquire = [&](uint32_t ps) -> bool {
+    return mbar_wait(ring.empty_bar(ps), ring.phase(ps) ^ 1u, abort);
+  };
+  auto load_nope = [&](const CUtensorMap* map, int x, const ItemInfo& it, int j) -> bool {
+    if (!acquire(pos)) return false;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(ring.full_bar(pos), kChunk);
+      tma_load_3d(ring.buf(pos), map, ring.full_bar(pos), x, it.h, it.kv_row0 + j * kBN);
+    }
+    ++pos;
+    return true;
+  };
+  auto load_rope = [&](const ItemInfo& it, int j) -> bool {
+    if (!acquire(pos)) return false;
+    const int key0 = j * kBN;
+    if (!p.rope_manual) {
+      // One TMA box of rope_box rows per page segment; lane t owns box t.
+      const int nbox = kBN / static_cast<int>(p.rope_box);
+      bool issue = false;
+      uint32_t page = 0, row_in_page = 0;
+      if (lane < nbox) {
+        const int key = key0 + lane * static_cast<int>(p.rope_box);
+        if (key < it.L) {
+          const uint32_t col = static_cast<uint32_t>(key) / p.page_size;
+          row_in_page = static_cast<uint32_t>(key) - col * p.page_size;
+          if (col >= p.max_pages) {
+            status |= MLA_DEVICE_STATUS_BAD_COLUMN;
+          } else {
+            page = p.page_table[static_cast<long long>(it.b) * p.pt_stride + col];
+            if (page >= p.num_pages) status |= MLA_DEVICE_STATUS_BAD_PAGE;
+            else issue = true;
+          }
+        }
+      }
+      const uint32_t mask = __ballot_sync(0xffffffffu, issue);
+      const uint32_t bytes = __popc(mask) * p.rope_box * 128u;
+      if (lane == 0) {
+        if (bytes) mbar_arrive_expect_tx(ring.full_bar(pos), bytes);
+        else mbar_arrive(ring.full_bar(pos));
+      }
+      __syncwarp();
+      if (issue)
+        tma_load_3d(ring.buf(pos) + lane * p.rope_box * 128u, &p.tm_rope, ring.full_bar(pos), 0,
+                    static_cast<int>(row_in_page), static_cast<int>(page));
+    } else {
+      // Row-by-row gather into the 128B-swizzled layout.
+      const uint32_t dst = ring.buf(pos);
+      for (int r = lane; r < kBN; r += 32) {
+        const int key = key0 + r;
+        if (key >= it.L) continue;
+        const uint32_t col = static_cast<uint32_t>(key) / p.page_size;
+        if (col >= p.max_pages) { status |= MLA_DEVICE_STATUS_BAD_COLUMN; continue; }
+        const uint32_t page = p.page_table[static_cast<long long>(it.b) * p.pt_stride + col];
+        if (page >= p.num_pages) { status |= MLA_DEVICE_STATUS_BAD_PAGE; continue; }
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.rope_base + page * p.rope_page_bytes +
+            static_cast<long long>(key - static_cast<int>(col * p.page_size)) * p.rope_tok_bytes);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = src[c];
+          const uint32_t a = dst + r * 128 + ((c ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+                       "r"(v.z), "r"(v.w)
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ring.full_bar(pos));
+    }
+    ++pos;
+    return true;
+  };
+  auto load_q = [&](int q, const ItemInfo& it) -> bool {
+    const uint32_t bar = smem_u32(&s.q_full[q]);
+    if (!mbar_wait(smem_u32(&s.q_empty[q]), (q_uses[q] & 1u) ^ 1u, abort)) return false;
+    ++q_uses[q];
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, 3 * kChunk);
+      for (int a = 0; a < 3; ++a)
+        tma_load_3d(smem_u32(&s.q[q][a][0]), &p.tm_q, bar, 64 * a, it.h, it.q_row0 + q * kBM);
+    }
+    return true;
+  };
+
+  while (alive) {
+    uint32_t t = 0;
+    if (lane == 0) t = atomicAdd(&hdr->counter, 1u);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    const ItemInfo it = decode_item(t, hdr, recs, p.H, p.causal);
+    const uint32_t islot = item_k & 1u;
+    if (!mbar_wait(smem_u32(&s.item_empty[islot]), ((item_k >> 1) & 1u) ^ 1u, abort)) break;
+    if (lane == 0) {
+      s.items[islot] = it;
+      mbar_arrive(smem_u32(&s.item_full[islot]));
+    }
+    ++item_k;
+    if (!it.valid) break;
+    const int nkv = it.n1 > 0 ? it.nkv1 : it.nkv0;
+    for (int j = 0; j < nkv && alive; ++j) {
+      alive = load_nope(&p.tm_k, 0, it, j) && load_nope(&p.tm_k, 64, it, j) && load_rope(it, j);
+      if (alive && j == 0) alive = load_q(0, it) && (it.n1 == 0 || load_q(1, it));
+      alive = alive && load_nope(&p.tm_v, 0, it, j) && load_nope(&p.tm_v, 64, it, j);
+    }
+  }
+  if (status) atomicOr(&hdr->status, status);
+  if (*abort) {
+    // Let every copy this warp started land before the CTA exits.
+    for (uint32_t ps = pos > kRing ? pos - kRing : 0; ps < pos; ++ps)
+      wait_drain(ring.full_bar(ps), ring.phase(ps));
+    for (int q = 0; q < 2; ++q)
+      if (q_uses[q]) wait_drain(smem_u32(&s.q_full[q]), (q_uses[q] - 1) & 1u);
+  }
+}
+
+__device__ void mma_thread(Smem& s, uint32_t tmem, volatile uint32_t* abort) {
+  const Ring ring{smem_u32(&s.kv_full[0]), smem_u32(&s.kv_empty[0]), smem_u32(&s.ring[0][0])};
+  const uint32_t idS = make_idesc(128, 128, 1, false);
+  const uint32_t idPV = make_idesc(128, 64, 1, true);
+  const uint32_t qbase[2] = {smem_u32(&s.q[0][0][0]), smem_u32(&s.q[1][0][0])};
+  uint32_t pos = 0, item_k = 0, qf[2] = {0, 0}, pf[2] = {0, 0}, oe[2] = {0, 0};
+  bool alive = true;
+
+  auto wait_chunks = [&](uint32_t first, int count) -> bool {
+    for (int c = 0; c < count; ++c)
+      if (!mbar_wait(ring.full_bar(first + c), ring.phase(first + c), abort)) return false;
+    tc_fence_after();
+    return true;
+  };
+  auto issue_s = [&](int q, uint32_t kpos) {
+#pragma unroll
+    for (int ks = 0; ks < 12; ++ks) {
+      const int a = ks >> 2;
+      const uint32_t off = (ks & 3) * 32;
+      const uint64_t ad = sw128_desc(qbase[q] + a * kChunk + off, 16, 1024);
+      const uint64_t bd = sw128_desc(ring.buf(kpos + a) + off, 16, 1024);
+      umma_f16_ss(tmem + col_s(q), ad, bd, idS, ks > 0);
+    }
+    umma_commit(smem_u32(&s.s_full[q]));
+  };
+  auto issue_pv = [&](int q, uint32_t vpos, bool acc) {
+    const uint32_t v0 = ring.buf(vpos), v1 = ring.buf(vpos + 1);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t a = tmem + col_s(q) + ks * 8;
+      umma_f16_ts(tmem + col_o(q), a, sw128_desc(v0 + ks * 2048, 16, 1024), idPV, acc || ks > 0);
+      umma_f16_ts(tmem + col_o(q) + 64, a, sw128_desc(v1 + ks * 2048, 16, 1024), idPV, acc || ks > 0);
+    }
+  };
+  auto release = [&](uint32_t first, int count) {
+    for (int c = 0; c < count; ++c) umma_commit(ring.empty_bar(first + c));
+  };
+  auto wait_p = [&](int q, bool first_tile) -> bool {
+    if (!mbar_wait(smem_u32(&s.p_full[q]), pf[q] & 1u, abort)) return false;
+    ++pf[q];
+    if (first_tile) {
+      if (!mbar_wait(smem_u32(&s.o_empty[q]), (oe[q] & 1u) ^ 1u, abort)) return false;
+      ++oe[q];
+    }
+    tc_fence_after();
+    return true;
+  };
+
+  while (alive) {
+    const uint32_t islot = item_k & 1u;
+    if (!mbar_wait(smem_u32(&s.item_full[islot]), (item_k >> 1) & 1u, abort)) break;
+    const ItemInfo it = s.items[islot];
+    mbar_arrive(smem_u32(&s.item_empty[islot]));
+    ++item_k;
+    if (!it.valid) break;
+    const bool has1 = it.n1 > 0;
+    const int nkv = has1 ? it.nkv1 : it.nkv0;
+    // Per tile j: K chunks at pos + 5j .. +2, V chunks at pos + 5j + 3 .. +4.
+    auto kpos = [&](int j) { return pos + kChunksPerTile * j; };
+    alive = wait_chunks(kpos(0), 3);
+    alive = alive && mbar_wait(smem_u32(&s.q_full[0]), qf[0] & 1u, abort);
+    ++qf[0];
+    if (alive && has1) {
+      alive = mbar_wait(smem_u32(&s.q_full[1]), qf[1] & 1u, abort);
+      ++qf[1];
+    }
+    if (!alive) break;
+    tc_fence_after();
+    issue_s(0, kpos(0));
+    if (has1) issue_s(1, kpos(0));
+    release(kpos(0), 3);
+    for (int j = 0; j < nkv && alive; ++j) {
+      const bool on0 = j < it.nkv0;
+      const bool next0 = j + 1 < it.nkv0;
+      const bool next1 = has1 && j + 1 < nkv;
+      bool k_next = false;  // K chunks of tile j+1 waited for
+      auto need_k_next = [&]() -> bool {
+        if (k_next) return true;
+        k_next = true;
+        return wait_chunks(kpos(j + 1), 3);
+      };
+      if (!(alive = wait_chunks(kpos(j) + 3, 2))) break;
+      if (on0) {
+        if (!(alive = wait_p(0, j == 0))) break;
+        issue_pv(0, kpos(j) + 3, j > 0);
+        if (next0) {
+          if (!(alive = need_k_next())) break;
+          issue_s(0, kpos(j + 1));
+        } else {
+          umma_commit(smem_u32(&s.o_full[0]));
+          umma_commit(smem_u32(&s.q_empty[0]));
+        }
+      }
+      if (has1) {
+        if (!(alive = wait_p(1, j == 0))) break;
+        issue_pv(1, kpos(j) + 3, j > 0);
+        release(kpos(j) + 3, 2);
+        if (next1) {
+          if (!(alive = need_k_next())) break;
+          issue_s(1, kpos(j + 1));
+        } else {
+          umma_commit(smem_u32(&s.o_full[1]));
+          umma_commit(smem_u32(&s.q_empty[1]));
+        }
+      } else {
+        release(kpos(j) + 3, 2);
+      }
+      if (next0 || next1) release(kpos(j + 1), 3);
+    }
+    pos += kChunksPerTile * nkv;
+  }
+  // Make sure no UMMA is still in flight before tensor memory is released.
+  umma_commit(smem_u32(&s.drain));
+  wait_drain(smem_u32(&s.drain), 0);
+}
+
+__device__ void softmax_warp(Smem& s, const AttnParams& p, uint32_t tmem, int q, int wq, int lane,
+                             volatile uint32_t* abort) {
+  const int r = wq * 32 + lane;  // query row inside the tile == TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t t_s = tmem + lane_off + col_s(q);
+  const uint32_t t_o = tmem + lane_off + col_o(q);
+  const float sl2 = p.sl2;
+  uint32_t item_k = 0, sf = 0, of = 0;
+
+  for (;;) {
+    const uint32_t islot = item_k & 1u;
+    if (!mbar_wait(smem_u32(&s.item_full[islot]), (item_k >> 1) & 1u, abort)) return;
+    const ItemInfo it = s.items[islot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.item_empty[islot]));
+    ++item_k;
+    if (!it.valid) return;
+    if (q == 1 && it.n1 == 0) continue;
+    const int nkv = q ? it.nkv1 : it.nkv0;
+    const int i = it.i0 + q * kBM + r;  // query index inside the sequence
+    const int last_key = it.L - 1;
+    const int limit = p.causal ? min(it.prior + i, last_key) : last_key;
+    const int tile_limit = p.causal ? min(it.prior + it.i0 + q * kBM, last_key) : last_key;
+    float m_used = -INFINITY, l = 0.f;
+
+    for (int j = 0; j < nkv; ++j) {
+      if (!mbar_wait(smem_u32(&s.s_full[q]), sf & 1u, abort)) return;
+      ++sf;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(t_s + 32 * c, sr[c]);
+      tmem_ld_wait();
+      const int key0 = j * kBN;
+      const bool masked = key0 + kBN - 1 > tile_limit;
+      float smax = -INFINITY;
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const bool ok = key0 + 32 * c + e <= limit;
+            const float v = ok ? __uint_as_float(sr[c][e]) : -INFINITY;
+            sr[c][e] = __float_as_uint(v);
+            smax = fmaxf(smax, v);
+          }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) smax = fmaxf(smax, __uint_as_float(sr[c][e]));
+      }
+      const float m_tile = smax == -INFINITY ? -INFINITY : smax * sl2;
+      const float m_new = fmaxf(m_used, m_tile);
+      const bool grow = m_new > m_used + kRescaleThreshold;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2_approx(m_used - m_new);
+        m_used = m_new;
+        l *= alpha;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[16];
+          tmem_ld_32x32b_x16(t_o + 16 * c, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_32x32b_x16(t_o + 16 * c, o);
+        }
+      }
+      const float mb = m_used == -INFINITY ? 0.f : m_used;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float s0 = __uint_as_float(sr[c][2 * e]), s1 = __uint_as_float(sr[c][2 * e + 1]);
+          float p0 = ex2_approx(fmaf(s0, sl2, -mb));
+          float p1 = ex2_approx(fmaf(s1, sl2, -mb));
+          if (masked) {
+            p0 = s0 == -INFINITY ? 0.f : p0;
+            p1 = s1 == -INFINITY ? 0.f : p1;
+          }
+          l += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_32x32b_x16(t_s + 16 * c, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s.p_full[q]));
+    }
+
+    // Epilogue: O / l -> bf16 rows of out.
+    if (!mbar_wait(smem_u32(&s.o_full[q]), of & 1u, abort)) return;
+    ++of;
+    tc_fence_after();
+    const float inv = 1.f / l;
+    const bool store = i < it.n;
+    uint4* dst = reinterpret_cast<uint4*>(
+        p.out + static_cast<long long>(it.q_row0 + q * kBM + r) * p.out_tok +
+        static_cast<long long>(it.h) * p.out_head);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[32];
+      tmem_ld_32x32b_x32(t_o + 32 * c, o);
+      tmem_ld_wait();
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+      if (store) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[4 * c + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.o_empty[q]));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile uint32_t* abort = &s.abort_flag;
+
+  if (threadIdx.x == 0) {
+    s.abort_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.item_full[i]), 1);
+      mbar_init(smem_u32(&s.item_empty[i]), 9);  // MMA thread + 8 softmax warps
+      mbar_init(smem_u32(&s.q_full[i]), 1);
+      mbar_init(smem_u32(&s.q_empty[i]), 1);
+      mbar_init(smem_u32(&s.s_full[i]), 1);
+      mbar_init(smem_u32(&s.p_full[i]), 4);
+      mbar_init(smem_u32(&s.o_full[i]), 1);
+      mbar_init(smem_u32(&s.o_empty[i]), 4);
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(smem_u32(&s.kv_full[i]), 1);
+      mbar_init(smem_u32(&s.kv_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&s.drain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+    if (!p.rope_manual) tma_prefetch_desc(&p.tm_rope);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp == 0) {
+    producer_warp(s, p, lane, abort);
+  } else if (warp == 1) {
+    if (lane == 0) mma_thread(s, tmem, abort);
+    __syncwarp();
+  } else if (warp >= 4) {
+    softmax_warp(s, p, tmem, (warp - 4) >> 2, warp & 3, lane, abort);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && s.abort_flag)
+    atomicOr(&reinterpret_cast<WsHeader*>(p.ws)->status, MLA_DEVICE_STATUS_TIMEOUT);
+}
+
+// ------------------------------------------------------------ host side
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+mla_status_t check_tensor(const mla_tensor_t* t, const char* name, int ndim, mla_dtype_t dtype) {
+  if (!t) return fail(MLA_ERR_INVALID_ARG, "%s descriptor is NULL", name);
+  if (!t->data) return fail(MLA_ERR_INVALID_ARG, "%s data is NULL", name);
+  if (t->ndim != ndim) return fail(MLA_ERR_INVALID_ARG, "%s has ndim %d, expected %d", name, t->ndim, ndim);
+  if (t->dtype != dtype) return fail(MLA_ERR_INVALID_ARG, "%s has dtype %d, expected %d", name, (int)t->dtype, (int)dtype);
+  for (int i = 0; i < ndim; ++i) {
+    if (t->shape[i] < 0 || t->shape[i] > 0x7FFFFFFFll)
+      return fail(MLA_ERR_INVALID_ARG, "%s shape[%d] = %lld out of range", name, i, (long long)t->shape[i]);
+    if (t->stride[i] < 0) return fail(MLA_ERR_INVALID_ARG, "%s stride[%d] is negative", name, i);
+  }
+  if (t->stride[ndim - 1] != 1) return fail(MLA_ERR_INVALID_ARG, "%s innermost stride must be 1", name);
+  return MLA_OK;
+}
+
+}  // namespace
+}  // namespace mla
+
+extern "C" size_t mla_prefill_ragged_workspace_size(uint32_t batch) {
+  size_t bytes = sizeof(mla::WsHeader) + static_cast<size_t>(batch) * sizeof(mla::SeqRec);
+  return (bytes + 255) & ~size_t(255);
+}
+
+extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_tensor_t* q,
+                                           const mla_tensor_t* k_nope, const mla_tensor_t* v,
+                                           const mla_tensor_t* k_rope_pages,
+                                           const mla_tensor_t* page_table,
+                                           const uint32_t* row_offsets, const uint32_t* cache_lens,
+                                           float scale, mla_mask_t mask, void* workspace,
+                                           size_t workspace_bytes, mla_stream_t stream) {
+  using namespace mla;
+  mla_status_t st;
+  if (!q) return fail(MLA_ERR_INVALID_ARG, "q descriptor is NULL");
+  if (q->dtype == MLA_DTYPE_FP8_E4M3)
+    return fail(MLA_ERR_UNSUPPORTED, "fp8 inputs are not built into this library version");
+  const mla_dtype_t dt = MLA_DTYPE_BF16;
+  if ((st = check_tensor(q, "q", 3, dt)) != MLA_OK) return st;
+  if ((st = check_tensor(out, "out", 3, MLA_DTYPE_BF16)) != MLA_OK) return st;
+  if ((st = check_tensor(k_nope, "k_nope", 3, dt)) != MLA_OK) return st;
+  if ((st = check_tensor(v, "v", 3, dt)) != MLA_OK) return st;
+  if ((st = check_tensor(k_rope_pages, "k_rope_pages", 3, dt)) != MLA_OK) return st;
+  if ((st = check_tensor(page_table, "page_table", 2, MLA_DTYPE_U32)) != MLA_OK) return st;
+  if (!row_offsets || !cache_lens) return fail(MLA_ERR_INVALID_ARG, "row_offsets / cache_lens is NULL");
+  if (mask != MLA_MASK_CAUSAL && mask != MLA_MASK_NULL) return fail(MLA_ERR_INVALID_ARG, "unknown mask %d", (int)mask);
+  if (!(scale >= 0.f) || !std::isfinite(scale)) return fail(MLA_ERR_INVALID_ARG, "scale must be finite and >= 0");
+
+  const int64_t Tq = q->shape[0], H = q->shape[1], Sk = k_nope->shape[0];
+  const int64_t B = page_table->shape[0], max_pages = page_table->shape[1];
+  const int64_t NP = k_rope_pages->shape[0], P = k_rope_pages->shape[1];
+  if (q->shape[2] != 192) return fail(MLA_ERR_INVALID_ARG, "q depth must be 192");
+  if (out->shape[0] != Tq || out->shape[1] != H || out->shape[2] != 128)
+    return fail(MLA_ERR_INVALID_ARG, "out must be [Tq, H, 128] matching q");
+  if (k_nope->shape[1] != H || k_nope->shape[2] != 128) return fail(MLA_ERR_INVALID_ARG, "k_nope must be [Sk, H, 128]");
+  if (v->shape[0] != Sk || v->shape[1] != H || v->shape[2] != 128) return fail(MLA_ERR_INVALID_ARG, "v must be [Sk, H, 128] matching k_nope");
+  if (k_rope_pages->shape[2] != 64) return fail(MLA_ERR_INVALID_ARG, "k_rope_pages must be [num_pages, P, 64]");
+  if (H < 1) return fail(MLA_ERR_INVALID_ARG, "num_heads must be >= 1");
+  if (B < 1 || B > kMaxBatch) return fail(MLA_ERR_INVALID_ARG, "batch %lld outside 1..%u", (long long)B, kMaxBatch);
+  if (P < 1 || NP < 1 || max_pages < 1) return fail(MLA_ERR_INVALID_ARG, "empty page pool or page table");
+  if (NP * P > 0x7FFFFFFFll) return fail(MLA_ERR_INVALID_ARG, "page pool exceeds 2^31 slots");
+  if (Sk < Tq) return fail(MLA_ERR_INVALID_ARG, "k_nope has fewer rows than q");
+  if ((Tq / kQRows + B + 1) * H > 0x7FFFFFFFll)
+    return fail(MLA_ERR_INVALID_ARG, "too many work items (query blocks x heads exceeds 2^31)");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(MLA_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
+  if (workspace_bytes < mla_prefill_ragged_workspace_size(static_cast<uint32_t>(B)))
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small");
+  // TMA and vector-store constraints: 16-byte aligned bases and strides.
+  const mla_tensor_t* ts[5] = {q, k_nope, v, k_rope_pages, out};
+  const char* names[5] = {"q", "k_nope", "v", "k_rope_pages", "out"};
+  for (int i = 0; i < 5; ++i) {
+    if (!aligned16(ts[i]->data)) return fail(MLA_ERR_INVALID_ARG, "%s data must be 16-byte aligned", names[i]);
+    for (int d = 0; d < 2; ++d)
+      if ((ts[i]->stride[d] * 2) % 16 != 0 || ts[i]->stride[d] * 2 >= (1ll << 40))
+        return fail(MLA_ERR_INVALID_ARG, "%s stride[%d] must be a multiple of 8 elements", names[i], d);
+  }
+
+  int dev = 0, sms = 0;
+  if ((st = check_device(&dev, &sms)) != MLA_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (Tq == 0) {
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(WsHeader), cs);
+    if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "workspace reset: %s", cudaGetErrorString(e));
+    return MLA_OK;
+  }
+
+  AttnParams prm;
+  memset(&prm, 0, sizeof(prm));
+  {
+    uint64_t dims[3] = {192, (uint64_t)H, (uint64_t)Tq};
+    uint64_t str[2] = {(uint64_t)q->stride[1] * 2, (uint64_t)q->stride[0] * 2};
+    uint32_t box[3] = {64, 1, kBM};
+    if ((st = encode_tiled(&prm.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q->data, dims, str, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "q")) != MLA_OK)
+      return st;
+  }
+  {
+    uint64_t dims[3] = {128, (uint64_t)H, (uint64_t)Sk};
+    uint32_t box[3] = {64, 1, kBN};
+    uint64_t str[2] = {(uint64_t)k_nope->stride[1] * 2, (uint64_t)k_nope->stride[0] * 2};
+    if ((st = encode_tiled(&prm.tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_nope->data, dims, str, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "k_nope")) != MLA_OK)
+      return st;
+    uint64_t strv[2] = {(uint64_t)v->stride[1] * 2, (uint64_t)v->stride[0] * 2};
+    if ((st = encode_tiled(&prm.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v->data, dims, strv, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "v")) != MLA_OK)
+      return st;
+  }
+  uint32_t g = 1;
+  {
+    uint32_t a = static_cast<uint32_t>(P), b = kBN;
+    while (b) { uint32_t t = a % b; a = b; b = t; }
+    g = a;  // gcd(P, 128): rows per page segment inside a key tile
+  }
+  prm.rope_manual = (g % 8u) != 0;
+  prm.rope_box = g;
+  if (!prm.rope_manual) {
+    uint64_t dims[3] = {64, (uint64_t)P, (uint64_t)NP};
+    uint64_t str[2] = {(uint64_t)k_rope_pages->stride[1] * 2, (uint64_t)k_rope_pages->stride[0] * 2};
+    uint32_t box[3] = {64, g, 1};
+    if ((st = encode_tiled(&prm.tm_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_rope_pages->data, dims,
+                           str, box, CU_TENSOR_MAP_SWIZZLE_128B, "k_rope_pages")) != MLA_OK)
+      return st;
+  }
+  prm.out = static_cast<uint16_t*>(out->data);
+  prm.out_tok = out->stride[0];
+  prm.out_head = out->stride[1];
+  prm.page_table = static_cast<const uint32_t*>(page_table->data);
+  prm.pt_stride = page_table->stride[0];
+  prm.rope_base = static_cast<const uint8_t*>(k_rope_pages->data);
+  prm.rope_tok_bytes = k_rope_pages->stride[1] * 2;
+  prm.rope_page_bytes = k_rope_pages->stride[0] * 2;
+  prm.max_pages = static_cast<uint32_t>(max_pages);
+  prm.num_pages = static_cast<uint32_t>(NP);
+  prm.page_size = static_cast<uint32_t>(P);
+  prm.H = static_cast<uint32_t>(H);
+  prm.causal = mask == MLA_MASK_CAUSAL;
+  prm.sl2 = scale * 1.4426950408889634f;
+  prm.ws = static_cast<uint8_t*>(workspace);
+
+  const int sched_smem = static_cast<int>(3 * B * sizeof(uint32_t));
+  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(schedule_kernel), sched_smem, dev, 1)) != MLA_OK)
+    return st;
+  const int attn_smem = static_cast<int>(sizeof(Smem) + 1024);
+  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(mla_attention_kernel), attn_smem, dev, 2)) != MLA_OK)
+    return st;
+  schedule_kernel<<<1, kSchedThreads, sched_smem, cs>>>(
+      row_offsets, cache_lens, static_cast<uint32_t>(B), static_cast<uint32_t>(H),
+      static_cast<uint32_t>(Tq), static_cast<uint32_t>(Sk), static_cast<uint32_t>(P),
+      static_cast<uint32_t>(max_pages), 2u * (128 + 128), static_cast<uint8_t*>(workspace));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "scheduler launch: %s", cudaGetErrorString(e));
+  mla_attention_kernel<<<sms, kThreads, attn_smem, cs>>>(prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  return MLA_OK;
+}

@@ -1,0 +1,31 @@
+// Host-side helpers shared by the entry points: per-thread error text, the
+// device capability check and the tensor-map encoder.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+
+#include "../../include/mla_prefill.h"
+
+namespace mla {
+
+// Record a failure for mla_last_error_string() and return `status`.
+mla_status_t fail(mla_status_t status, const char* fmt, ...);
+mla_status_t ok();
+
+// Current device must be compute capability 10.3.  Fills the SM count.
+mla_status_t check_device(int* device_out, int* num_sms_out);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).  Returns MLA_ERR_CUDA when the encoder rejects the map.
+mla_status_t encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, void* base,
+                          const uint64_t* dims, const uint64_t* strides_bytes,
+                          const uint32_t* box, CUtensorMapSwizzle swizzle, const char* what);
+
+// Allow `bytes` of dynamic shared memory for `func` on `device` (cached).
+mla_status_t set_max_dynamic_smem(const void* func, int bytes, int device, int slot);
+
+}  // namespace mla

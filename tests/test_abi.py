@@ -1,0 +1,114 @@
+"""C-ABI library checks that need no GPU: it loads, exports every entry point
+declared in include/*.h, and rejects bad arguments on the host before touching
+the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import mla_ragged_paged_gb300 as pkg
+from mla_ragged_paged_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkg.build()
+    return binding.load()
+
+
+def _declared_functions():
+    names = set()
+    for path in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(mla_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert "mla_prefill_plan" in declared and "mla_prefill_ragged" in declared
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared but not exported"
+    assert sorted(binding.EXPORTS) == [n for n in declared if n in binding.EXPORTS]
+
+
+def test_host_helpers(lib):
+    assert binding.plan_max_rows(50, 32) == 2
+    assert binding.plan_max_rows(0, 32) == 0
+    assert binding.plan_max_rows(64, 32) == 2
+    assert binding.plan_max_rows(10, 0) == 0
+    ws = binding.workspace_size(8)
+    assert ws % 256 == 0 and ws >= 256 + 8 * 32
+
+
+def _desc(shape, dtype=binding.MLA_DTYPE_BF16, ptr=0x10000):
+    d = binding.MlaTensor()
+    d.data = ptr
+    d.dtype = dtype
+    d.ndim = len(shape)
+    stride = 1
+    for i in reversed(range(len(shape))):
+        d.shape[i] = shape[i]
+        d.stride[i] = stride
+        stride *= shape[i]
+    return d
+
+
+def _ragged_args(**over):
+    a = dict(out=_desc([10, 2, 128]), q=_desc([10, 2, 192]), k=_desc([20, 2, 128]),
+             v=_desc([20, 2, 128]), rope=_desc([4, 16, 64]),
+             pt=_desc([2, 2], binding.MLA_DTYPE_U32), ro=0x20000, cl=0x30000, scale=0.07,
+             mask=binding.MLA_MASK_CAUSAL, ws=0x40000, ws_bytes=4096)
+    a.update(over)
+    return a
+
+
+def _call_ragged(lib, a):
+    r = lambda d: None if d is None else ctypes.byref(d)
+    return lib.mla_prefill_ragged(r(a["out"]), r(a["q"]), r(a["k"]), r(a["v"]), r(a["rope"]),
+                                  r(a["pt"]), a["ro"], a["cl"], a["scale"], a["mask"], a["ws"],
+                                  a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("change", [
+    dict(q=None), dict(out=None), dict(ro=None), dict(cl=None), dict(ws=None),
+    dict(q=_desc([10, 2, 128])),                        # q depth must be 192
+    dict(out=_desc([10, 2, 64])),                       # output depth 128
+    dict(k=_desc([20, 3, 128])),                        # head count mismatch
+    dict(v=_desc([19, 2, 128])),                        # v rows differ from k
+    dict(rope=_desc([4, 16, 32])),                      # rope depth 64
+    dict(rope=_desc([0, 16, 64])),                      # empty pool
+    dict(pt=_desc([2, 2], binding.MLA_DTYPE_BF16)),     # page table dtype
+    dict(q=_desc([10, 2, 192], binding.MLA_DTYPE_U32)),  # q dtype
+    dict(scale=-1.0), dict(scale=float("nan")), dict(mask=7),
+    dict(ws=0x40008),                                   # workspace alignment
+    dict(ws_bytes=16),                                  # workspace size
+    dict(k=_desc([5, 2, 128]), v=_desc([5, 2, 128])),   # fewer K rows than Q rows
+    dict(q=_desc([10, 2, 192], ptr=0x10004)),            # unaligned base
+])
+def test_ragged_rejects_bad_arguments(lib, change):
+    assert _call_ragged(lib, _ragged_args(**change)) == binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_last_error_string()
+
+
+def test_ragged_rejects_unaligned_stride(lib):
+    q = _desc([10, 2, 192])
+    q.stride[1] = 196          # 392 bytes: not a multiple of 16
+    assert _call_ragged(lib, _ragged_args(q=q)) == binding.MLA_ERR_INVALID_ARG
+    assert b"stride" in lib.mla_last_error_string()
+
+
+def test_plan_rejects_bad_arguments(lib):
+    f = lib.mla_prefill_plan
+    P = 0x10000
+    assert f(None, P, 2, 32, 4, P, P, P, None, None) == binding.MLA_ERR_INVALID_ARG
+    assert f(P, None, 2, 32, 4, P, P, P, None, None) == binding.MLA_ERR_INVALID_ARG
+    assert f(P, P, 2, 0, 4, P, P, P, None, None) == binding.MLA_ERR_INVALID_ARG
+    assert f(P, P, 2, 32, 4, None, P, P, None, None) == binding.MLA_ERR_INVALID_ARG
+    assert f(P, P, 1 << 20, 32, 4, P, P, P, None, None) == binding.MLA_ERR_INVALID_ARG
+    assert b"buffer_token_size" in lib.mla_last_error_string() or lib.mla_last_error_string()

@@ -1,0 +1,126 @@
+"""GPU attention (mla_prefill_ragged through the C ABI) versus the float64
+oracle, element by element.
+
+Tolerance (bf16 inputs, bf16 output): |gpu - ref| <= 2e-2 + 2e-2 * |ref|.
+Small workloads are compared in full; the full-size workloads run in the same
+launch configuration as the benchmark and are compared on sampled rows and
+heads, which the oracle computes one (sequence, head) at a time.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import attention as oatt
+
+pytestmark = pytest.mark.gpu
+
+ATOL = RTOL = 2e-2
+
+
+def run_gpu(w, workspace=None):
+    from mla_ragged_paged_gb300 import binding
+    d = workloads.device_inputs(w)
+    out = torch.full((w.total_q, w.heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pool = d["k_rope_pool"][..., w.spec.rope_col:w.spec.rope_col + 64]
+    ws = binding.alloc_workspace(w.batch) if workspace is None else workspace
+    mask = binding.MLA_MASK_CAUSAL if w.spec.mask == "causal" else binding.MLA_MASK_NULL
+    binding.prefill_ragged(out, d["q"], d["k_nope"], d["v"], pool, d["page_table"],
+                           d["row_offsets"], d["cache_lens"], w.scale, mask, ws,
+                           q_scale=d.get("q_scale"), k_scale=d.get("k_scale"),
+                           v_scale=d.get("v_scale"), k_rope_scales=d.get("k_rope_scales"))
+    status = binding.device_status(ws)
+    return out.float().cpu().numpy().astype(np.float64), status
+
+
+def assert_close(got, ref, what, atol=ATOL, rtol=RTOL):
+    sel = ~np.isnan(ref)
+    assert sel.any()
+    g, r = got[sel], ref[sel]
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    err = np.abs(g - r)
+    bound = atol + rtol * np.abs(r)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} elements out of tolerance, "
+                           f"max err {err.max():.4g}, worst excess {(err - bound).max():.4g}")
+
+
+@pytest.mark.parametrize("name", ["tiny_bf16", "ragged_chunked_bf16"])
+def test_small_workloads_full(lib, name):
+    w = workloads.generate(workloads.config(name))
+    got, status = run_gpu(w)
+    assert status == 0
+    assert_close(got, oatt.reference(w), name)
+
+
+EDGE_CASES = {
+    "single_key": dict(n=[1], prior=[0]),
+    "ragged_tails": dict(n=[300, 0, 129, 256, 257, 1], prior=[0, 5, 1000, 127, 3, 77]),
+    "page_12_row_gather": dict(n=[150, 40], prior=[70, 0], page_size=12),
+    "page_24_boxes": dict(n=[200, 33], prior=[0, 260], page_size=24),
+    "page_256": dict(n=[300, 90], prior=[200, 0], page_size=256),
+    "latent_row_576": dict(n=[140, 60], prior=[10, 130], row_width=576, rope_col=512, page_size=64),
+    "null_mask": dict(n=[100, 130], prior=[50, 300], mask="null"),
+    "odd_heads": dict(n=[260, 20, 513], prior=[1, 0, 2], heads=3),
+    "zero_scale": dict(n=[70], prior=[20], value_scale=1.0),
+}
+
+
+@pytest.mark.parametrize("case", list(EDGE_CASES))
+def test_edge_cases(lib, case):
+    kw = dict(heads=2, page_size=16, seed=300 + list(EDGE_CASES).index(case))
+    kw.update(EDGE_CASES[case])
+    n, prior = kw.pop("n"), kw.pop("prior")
+    w = workloads.custom(n, prior, **kw)
+    if case == "zero_scale":
+        w.scale = 0.0
+    got, status = run_gpu(w)
+    assert status == 0
+    assert_close(got, oatt.reference(w), case)
+
+
+def test_many_sequences_random(lib):
+    rng = np.random.default_rng(77)
+    n = rng.integers(0, 300, size=40)
+    prior = rng.integers(0, 400, size=40) * (rng.random(40) < 0.5)
+    w = workloads.custom(n.tolist(), prior.tolist(), heads=4, page_size=32, seed=401)
+    got, status = run_gpu(w)
+    assert status == 0
+    assert_close(got, oatt.reference(w), "many_sequences")
+
+
+def test_repeat_calls_identical(lib):
+    w = workloads.custom([333, 77], [12, 500], heads=4, page_size=64, seed=402)
+    a, _ = run_gpu(w)
+    b, _ = run_gpu(w)
+    assert np.array_equal(a, b)
+
+
+def _sample_rows(w, per_seq=12, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = {}
+    for b in range(w.batch):
+        n = int(w.n[b])
+        if n == 0:
+            continue
+        fixed = [0, n - 1] + [x for x in (127, 128, 255, 256, 4095) if x < n]
+        rows[b] = np.unique(np.concatenate([fixed, rng.integers(0, n, size=per_seq)]))
+    return rows
+
+
+@pytest.mark.parametrize("name", ["deepseek_v3_bf16", "long_context_bf16"])
+def test_full_size_sampled(lib, name):
+    w = workloads.generate(workloads.config(name))
+    got, status = run_gpu(w)
+    assert status == 0
+    assert np.isfinite(got).all(), "every output row must be written and finite"
+    heads = [0, w.heads // 3, w.heads - 1]
+    ref = oatt.reference(w, heads=heads, rows=_sample_rows(w))
+    assert_close(got, ref, name)
+
+
+def test_bad_page_id_sets_status(lib):
+    w = workloads.custom([40], [100], heads=2, page_size=16, seed=403)
+    w.page_table[0, 3] = 10 ** 6          # no such page: the kernel skips it and flags it
+    _, status = run_gpu(w)
+    assert status & 0x1

@@ -283,3 +283,30 @@ def custom(n, prior, heads=2, page_size=16, dtype="bf16", seed=100, value_scale=
 
 def with_mask(spec: Spec, mask: str) -> Spec:
     return replace(spec, mask=mask)
+
+
+def device_inputs(w: Workload, device="cuda", pin=False):
+    """The workload's tensors on `device` (or pinned host memory when
+    device == "cpu" and pin=True): offsets and the page table as int32 holding
+    the uint32 values, fp8 scales as float32 tensors."""
+    def mv(t):
+        t = t.contiguous()
+        if device == "cpu":
+            return t.pin_memory() if pin else t
+        return t.to(device, non_blocking=True)
+
+    d = {
+        "q": mv(w.q),
+        "k_nope": mv(w.k_nope),
+        "v": mv(w.v),
+        "k_rope_pool": mv(w.k_rope_pool),
+        "page_table": mv(torch.from_numpy(w.page_table.astype(np.int32))),
+        "row_offsets": mv(torch.from_numpy(w.row_offsets.astype(np.int32))),
+        "cache_lens": mv(torch.from_numpy(w.cache_lens.astype(np.int32))),
+    }
+    if w.spec.dtype == "fp8":
+        d["q_scale"] = mv(torch.tensor([w.q_scale], dtype=torch.float32))
+        d["k_scale"] = mv(torch.tensor([w.k_scale], dtype=torch.float32))
+        d["v_scale"] = mv(torch.tensor([w.v_scale], dtype=torch.float32))
+        d["k_rope_scales"] = mv(w.k_rope_scales)
+    return d
