@@ -1,0 +1,340 @@
+"""Throughput benchmark for libmla_prefill (one JSON line on rank 0).
+
+A step is one pass of the whole path on one batch: the prefill plan followed
+by the ragged paged MLA attention, on the DeepSeek-V3-shaped workload (B=8,
+new lengths U[512,4096], no prior cache, H=128, q_depth 192, depth 128,
+k_rope 64 paged with P=128, causal, bf16).  Inputs are resident in HBM and
+larger than L2 (about 2.1 GB per batch), so no flush is needed between steps.
+
+Metric: causal-effective TFLOP/s = H * 2 * (192 + 128) * sum_b A_b per step,
+A_b = n_b * prior_b + n_b (n_b + 1) / 2 (the visible (query, key) pairs), over
+the device time of the timed steps.  Under torchrun every rank runs its own
+batch (weak scaling, no data-path collective); the step time is the maximum
+over ranks.
+
+--impl reference times the CPU oracle instead (float64, the machine's host
+cores) on a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+from dataclasses import replace
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "MLA prefill causal-effective TFLOP/s and % of GB300 tensor peak, 1 GPU"
+WORKLOAD = "deepseek_v3_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic of one attention launch on this workload, from the ncu capture
+# summarised in profiles/; valid only while the kernel source is unchanged.
+ATTENTION_TRAFFIC = {"source_sha1": None, "bytes_per_launch": None}
+
+
+def causal_flops(w):
+    pairs = 0
+    for b in range(w.batch):
+        n, prior = int(w.n[b]), int(w.prior[b])
+        pairs += n * prior + n * (n + 1) // 2 if w.spec.mask == "causal" else n * (n + prior)
+    return w.heads * 2 * (192 + 128) * pairs
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def source_sha1():
+    with open(os.path.join(ROOT, "mla_ragged_paged_gb300", "csrc", "attention.cu"), "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap,utilization.gpu")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:7], float(parts[7])))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        loaded = [r for r in rows if r[3] > 50] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[2]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(loaded)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def dist_max(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def oracle_sample(w, rows, head):
+    """Time the oracle on the last `rows` query rows of the longest sequence
+    of `w` for one head; returns (causal-effective flops, seconds, text)."""
+    from oracle import attention as oatt
+    b = int(np.argmax(w.n))
+    n, prior = int(w.n[b]), int(w.prior[b])
+    rows = int(min(n, max(1, rows)))
+    sel = np.arange(n - rows, n)
+    t0 = time.perf_counter()
+    oatt.reference(w, heads=[head % w.heads], rows={b: sel})
+    dt = time.perf_counter() - t0
+    pairs = int(sum(prior + i + 1 for i in sel)) if w.spec.mask == "causal" else rows * (n + prior)
+    text = f"sequence {b} (n={n}, prior={prior}), head {head % w.heads}, last {rows} query rows"
+    return 2 * (192 + 128) * pairs, dt, text
+
+
+def oracle_rows_for(w, budget_s):
+    """Query-row count for which one oracle_sample call takes about budget_s."""
+    _, dt, _ = oracle_sample(w, 256, 0)
+    return max(1, int(256 * budget_s / max(dt, 1e-4)))
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = workloads.generate(workloads.config(WORKLOAD))
+    per_step = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    rows = oracle_rows_for(w, per_step)
+    for i in range(args.warmup):
+        oracle_sample(w, rows, i)
+    tot_f, tot_t, sample = 0, 0.0, ""
+    for i in range(args.steps):
+        f, dt, sample = oracle_sample(w, rows, args.warmup + i)
+        tot_f += f
+        tot_t += dt
+    value = tot_f / tot_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_per_step": "query rows of one (sequence, head)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(),
+                             "kind": "oracle", "sample": f"per step: {sample}"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import mla_ragged_paged_gb300 as pkg
+    from mla_ragged_paged_gb300 import binding
+    pkg.build()
+    binding.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    spec = workloads.config(WORKLOAD)
+    w = workloads.generate(spec if rank == 0 else replace(spec, seed=spec.seed + 1000 * rank))
+    F = causal_flops(w)
+    d = workloads.device_inputs(w, device=dev)
+    Tq, H, B = w.total_q, w.heads, w.batch
+    T = spec.buffer_token_size
+    R = (w.total_k + T - 1) // T
+    out = torch.empty((Tq, H, 128), dtype=torch.bfloat16, device=dev)
+    ws = binding.alloc_workspace(B, dev)
+    plan_out = (torch.empty((R, B + 1), dtype=torch.int32, device=dev),
+                torch.empty((R, B), dtype=torch.int32, device=dev),
+                torch.empty((R,), dtype=torch.int32, device=dev),
+                torch.empty((1,), dtype=torch.int32, device=dev))
+    stream = torch.cuda.current_stream(dev)
+
+    def step(inp, o):
+        binding.plan(inp["row_offsets"], inp["cache_lens"], T, R, stream=stream, out=plan_out)
+        binding.prefill_ragged(o, inp["q"], inp["k_nope"], inp["v"], inp["k_rope_pool"],
+                               inp["page_table"], inp["row_offsets"], inp["cache_lens"], w.scale,
+                               binding.MLA_MASK_CAUSAL, ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step(d, out)
+    assert binding.device_status(ws) == 0, "device status after warm-up"
+
+    # Device-resident timing: per-step events around the attention call and
+    # around the whole step, on the launching stream.
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            binding.plan(d["row_offsets"], d["cache_lens"], T, R, stream=stream, out=plan_out)
+            ev[i][1].record(stream)
+            binding.prefill_ragged(out, d["q"], d["k_nope"], d["v"], d["k_rope_pool"],
+                                   d["page_table"], d["row_offsets"], d["cache_lens"], w.scale,
+                                   binding.MLA_MASK_CAUSAL, ws, stream=stream)
+            ev[i][2].record(stream)
+        t_end.record(stream)
+        barrier(world)
+    total_ms = dist_max(t_start.elapsed_time(t_end), world)
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    assert binding.device_status(ws) == 0, "device status after timed steps"
+    clocks = clk.summary()
+
+    # End to end through the public API: pinned host inputs -> device, plan +
+    # attention, output -> pinned host, every step.
+    h = workloads.device_inputs(w, device="cpu", pin=True)
+    keys = ["q", "k_nope", "v", "k_rope_pool", "page_table", "row_offsets", "cache_lens"]
+    d2 = {k: torch.empty_like(d[k]) for k in keys}
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(h[k].numel() * h[k].element_size() for k in keys)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k in keys:
+            d2[k].copy_(h[k], non_blocking=True)
+        step(d2, out)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier(world)
+    e2e_ms = dist_max(e0.elapsed_time(e1), world)
+
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    achieved = F / (attn_ms * 1e-3) / 1e12
+    traffic = None
+    if ATTENTION_TRAFFIC["source_sha1"] == source_sha1():
+        traffic = ATTENTION_TRAFFIC["bytes_per_launch"]
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        f, dt, sample = oracle_sample(w, oracle_rows_for(w, 12.0), 0)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+               "sample": sample + f"; {dt:.1f} s of float64 numpy on the host"}
+
+    if rank == 0:
+        value = world * F * args.steps / (total_ms * 1e-3) / 1e12
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD}: {spec.description}", "global_batch": B * world,
+                       "total_q_tokens": Tq, "heads": H, "causal_effective_tflop_per_step": F / 1e12,
+                       "parallelism": f"dp{world} (independent batches)" if world > 1 else "none",
+                       "l2": "inputs (2.1 GB) larger than L2; no flush",
+                       "step": "mla_prefill_plan + mla_prefill_ragged"},
+            "pct_of_peak": 100.0 * value / world / peak,
+            "clocks": clocks,
+            "e2e": {"value": world * F * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "mla_attention_kernel (+ its 1-CTA scheduler launch in the span)",
+                         "peak_source": f"{peak_src} bf16_tflops (burst)"},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

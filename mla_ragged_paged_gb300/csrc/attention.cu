@@ -11,12 +11,18 @@
 // GEMMs.  K_rope (64 dims shared by every head) is fetched from the paged
 // pool through the page table, one TMA box per page segment.
 //
-// Warp roles (384 threads):
+// Warp roles (384 threads = three warpgroups, one warp of each per SM
+// sub-partition):
 //   warp 0      producer: work-item fetch (atomic counter), TMA loads
 //   warp 1      UMMA issuer (one thread) and tensor-memory owner
 //   warps 2-3   idle
-//   warps 4-7   softmax + epilogue for Q0 (TMEM lanes 0..127)
+//   warps 4-7   softmax + epilogue for Q0
 //   warps 8-11  softmax + epilogue for Q1
+// A warp may only touch TMEM lanes 32*(warp%4) .. +31, so each softmax
+// warpgroup covers the 128 rows of its tile exactly once.  The kernel is
+// built for 168 registers per thread; warpgroup 0 then gives registers back
+// (setmaxnreg 120) so each softmax thread can hold its whole 128-column S row
+// (setmaxnreg 192): 120 + 2 * 192 = 3 * 168 per sub-partition.
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,384)
 // O1 [384,512); P_q is written as packed bf16 over the first 64 columns of S_q.
 // Shared memory: Q0/Q1 (3 x 16 KB each, 128B-swizzled K-major) and a ring of
@@ -41,6 +47,7 @@ constexpr int kChunk = 16384;     // 128 rows x 128 bytes
 constexpr int kRing = 8;
 constexpr int kChunksPerTile = 5;
 constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;  // registers per thread the register split assumes
 constexpr uint32_t kTmemCols = 512;
 // Tensor-memory column of S_q / O_q.
 __device__ __forceinline__ uint32_t col_s(int q) { return q ? 128u : 0u; }
@@ -531,6 +538,7 @@ __device__ void softmax_warp(Smem& s, const AttnParams& p, uint32_t tmem, int q,
   const uint32_t t_s = tmem + lane_off + col_s(q);
   const uint32_t t_o = tmem + lane_off + col_o(q);
   const float sl2 = p.sl2;
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
   uint32_t item_k = 0, sf = 0, of = 0;
 
   for (;;) {
@@ -559,23 +567,21 @@ __device__ void softmax_warp(Smem& s, const AttnParams& p, uint32_t tmem, int q,
       tmem_ld_wait();
       const int key0 = j * kBN;
       const bool masked = key0 + kBN - 1 > tile_limit;
-      float smax = -INFINITY;
+      // Columns c < nvalid are visible to this row.
+      const int nvalid = masked ? max(0, min(kBN, limit - key0 + 1)) : kBN;
       if (masked) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const bool ok = key0 + 32 * c + e <= limit;
-            const float v = ok ? __uint_as_float(sr[c][e]) : -INFINITY;
-            sr[c][e] = __float_as_uint(v);
-            smax = fmaxf(smax, v);
-          }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) smax = fmaxf(smax, __uint_as_float(sr[c][e]));
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e >= nvalid) sr[c][e] = __float_as_uint(-INFINITY);
       }
+      float smax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          smax = max3(smax, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
       const float m_tile = smax == -INFINITY ? -INFINITY : smax * sl2;
       const float m_new = fmaxf(m_used, m_tile);
       const bool grow = m_new > m_used + kRescaleThreshold;
@@ -585,34 +591,50 @@ __device__ void softmax_warp(Smem& s, const AttnParams& p, uint32_t tmem, int q,
         m_used = m_new;
         l *= alpha;
       }
+      const float mb = m_used == -INFINITY ? 0.f : m_used;
+      const uint64_t negm = f2_pack(-mb, -mb);
+      uint64_t lacc = f2_pack(0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int col = 32 * c + 2 * e;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])),
+                           sl2x2, negm), x0, x1);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if (masked) {
+            p0 = col < nvalid ? p0 : 0.f;
+            p1 = col + 1 < nvalid ? p1 : 0.f;
+          }
+          const uint64_t pp = f2_pack(p0, p1);
+          lacc = f2_add(lacc, pp);
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_32x32b_x16(t_s + 16 * c, pk);
+      }
+      float l0, l1;
+      f2_unpack(lacc, l0, l1);
+      l += l0 + l1;
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // The previous P.V of this tile has completed (it was issued before
+        // the S GEMM whose completion we just waited for).
+        const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t o[16];
           tmem_ld_32x32b_x16(t_o + 16 * c, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          for (int e = 0; e < 16; e += 2) {
+            float x0, x1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), x0, x1);
+            o[e] = __float_as_uint(x0);
+            o[e + 1] = __float_as_uint(x1);
+          }
           tmem_st_32x32b_x16(t_o + 16 * c, o);
         }
-      }
-      const float mb = m_used == -INFINITY ? 0.f : m_used;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float s0 = __uint_as_float(sr[c][2 * e]), s1 = __uint_as_float(sr[c][2 * e + 1]);
-          float p0 = ex2_approx(fmaf(s0, sl2, -mb));
-          float p1 = ex2_approx(fmaf(s1, sl2, -mb));
-          if (masked) {
-            p0 = s0 == -INFINITY ? 0.f : p0;
-            p1 = s1 == -INFINITY ? 0.f : p1;
-          }
-          l += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st_32x32b_x16(t_s + 16 * c, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -625,6 +647,7 @@ __device__ void softmax_warp(Smem& s, const AttnParams& p, uint32_t tmem, int q,
     ++of;
     tc_fence_after();
     const float inv = 1.f / l;
+    const uint64_t inv2 = f2_pack(inv, inv);
     const bool store = i < it.n;
     uint4* dst = reinterpret_cast<uint4*>(
         p.out + static_cast<long long>(it.q_row0 + q * kBM + r) * p.out_tok +
@@ -636,8 +659,11 @@ __device__ void softmax_warp(Smem& s, const AttnParams& p, uint32_t tmem, int q,
       tmem_ld_wait();
       uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+      for (int e = 0; e < 16; ++e) {
+        float x0, x1;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2), x0, x1);
+        pk[e] = pack_bf16x2(x0, x1);
+      }
       if (store) {
 #pragma unroll
         for (int v = 0; v < 4; ++v)
@@ -690,12 +716,16 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
 
-  if (warp == 0) {
-    producer_warp(s, p, lane, abort);
-  } else if (warp == 1) {
-    if (lane == 0) mma_thread(s, tmem, abort);
-    __syncwarp();
-  } else if (warp >= 4) {
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
+    if (warp == 0) {
+      producer_warp(s, p, lane, abort);
+    } else if (warp == 1) {
+      if (lane == 0) mma_thread(s, tmem, abort);
+      __syncwarp();
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
     softmax_warp(s, p, tmem, (warp - 4) >> 2, warp & 3, lane, abort);
   }
 
@@ -853,6 +883,20 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
   const int sched_smem = static_cast<int>(3 * B * sizeof(uint32_t));
   if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(schedule_kernel), sched_smem, dev, 1)) != MLA_OK)
     return st;
+  {
+    // The register split inside the kernel is only safe when the kernel was
+    // built with exactly kLaunchRegs registers per thread.
+    static int checked[64] = {0};
+    if (dev < 64 && !checked[dev]) {
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(&fa, mla_attention_kernel);
+      if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
+      if (fa.numRegs != kLaunchRegs)
+        return fail(MLA_ERR_UNSUPPORTED, "attention kernel built with %d registers per thread, expected %d",
+                    fa.numRegs, kLaunchRegs);
+      checked[dev] = 1;
+    }
+  }
   const int attn_smem = static_cast<int>(sizeof(Smem) + 1024);
   if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(mla_attention_kernel), attn_smem, dev, 2)) != MLA_OK)
     return st;
