@@ -153,7 +153,7 @@ size_t mla_prefill_ragged_workspace_size(uint32_t batch);
  * page-table column makes the kernel skip that load and set a status bit
  * (MLA_DEVICE_STATUS_*) instead of faulting.
  * Two launches (a one-CTA scheduler, then the persistent attention kernel);
- * no host synchronisation; usable under stream capture.
+ * no host synchronisation.
  */
 mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_tensor_t* q,
                                 const mla_tensor_t* k_nope, const mla_tensor_t* v,
@@ -161,6 +161,35 @@ mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_tensor_t* q,
                                 const uint32_t* row_offsets, const uint32_t* cache_lens,
                                 float scale, mla_mask_t mask, void* workspace,
                                 size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * mla_prefill_ragged for callers that cannot allocate device memory.  No
+ * counterpart on the reference pages: it exists for callers such as a plug-in
+ * whose host framework owns all device memory and offers it no scratch
+ * buffer, or a latency-critical path that may not call cudaMalloc (which can
+ * synchronise the device).  Arguments and results are those of
+ * mla_prefill_ragged without `workspace` / `workspace_bytes`; the caller still
+ * passes every input and output.
+ *   - The scheduler workspace is a fixed device array inside the library
+ *     (33,024 bytes, room for 1024 sequences) that every GPU loading the
+ *     library keeps until process exit.  A batch above 1024 returns
+ *     MLA_ERR_INVALID_ARG.
+ *   - The first call on a device looks the array's address up with
+ *     cudaGetSymbolAddress (one-time set-up with that device current); make
+ *     that first call before any stream capture.  Later calls only launch.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.
+ *   - All calls share the one array and each call rewrites what it needs, so
+ *     calls whose kernels can overlap on the GPU (different streams without
+ *     ordering between them) race and must not be issued.
+ *   - The device status word of these calls stays inside the library and is
+ *     not readable through mla_read_device_status.
+ */
+mla_status_t mla_prefill_ragged_noalloc(const mla_tensor_t* out, const mla_tensor_t* q,
+                                        const mla_tensor_t* k_nope, const mla_tensor_t* v,
+                                        const mla_tensor_t* k_rope_pages,
+                                        const mla_tensor_t* page_table,
+                                        const uint32_t* row_offsets, const uint32_t* cache_lens,
+                                        float scale, mla_mask_t mask, mla_stream_t stream);
 
 /* Device status bits written into the workspace's first uint32. */
 #define MLA_DEVICE_STATUS_BAD_PAGE 0x1u    /* page id >= num_pages */

@@ -20,7 +20,8 @@ STATUS_BITS = {0x1: "BAD_PAGE", 0x2: "BAD_COLUMN", 0x4: "BAD_OFFSETS", 0x8: "TIM
 
 # Names exported by the C ABI (kept in step with include/mla_prefill.h).
 EXPORTS = ["mla_prefill_plan", "mla_prefill_plan_max_rows", "mla_prefill_ragged_workspace_size",
-           "mla_prefill_ragged", "mla_read_device_status", "mla_last_error_string"]
+           "mla_prefill_ragged", "mla_prefill_ragged_noalloc", "mla_read_device_status",
+           "mla_last_error_string"]
 
 
 class MlaError(RuntimeError):
@@ -57,6 +58,9 @@ def load(path=LIB_PATH):
     lib.mla_prefill_ragged.argtypes = [pt, pt, pt, pt, pt, pt, vp, vp, ctypes.c_float, ctypes.c_int,
                                        vp, ctypes.c_size_t, vp]
     lib.mla_prefill_ragged.restype = ctypes.c_int
+    lib.mla_prefill_ragged_noalloc.argtypes = [pt, pt, pt, pt, pt, pt, vp, vp, ctypes.c_float,
+                                               ctypes.c_int, vp]
+    lib.mla_prefill_ragged_noalloc.restype = ctypes.c_int
     lib.mla_read_device_status.argtypes = [vp, ctypes.POINTER(u32), vp]
     lib.mla_read_device_status.restype = ctypes.c_int
     lib.mla_last_error_string.argtypes = []
@@ -158,6 +162,26 @@ def prefill_ragged(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cac
                                   ctypes.byref(d_v), ctypes.byref(d_r), ctypes.byref(d_pt),
                                   _ptr(row_offsets), _ptr(cache_lens), float(scale), int(mask),
                                   _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def prefill_ragged_noalloc(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,
+                           scale, mask=MLA_MASK_CAUSAL, stream=None):
+    """mla_prefill_ragged_noalloc (bf16 inputs): the same attention without a
+    caller workspace, for callers that cannot allocate device memory; the
+    library's built-in workspace holds up to 1024 sequences and is shared by
+    every call, so calls must not overlap on the GPU."""
+    lib = load()
+    d_out = describe(out, MLA_DTYPE_BF16)
+    d_q = describe(q, _dtype_code(q))
+    d_k = describe(k_nope, _dtype_code(k_nope))
+    d_v = describe(v, _dtype_code(v))
+    d_r = describe(k_rope_pages, _dtype_code(k_rope_pages))
+    d_pt = describe(page_table, MLA_DTYPE_U32)
+    _check(lib.mla_prefill_ragged_noalloc(ctypes.byref(d_out), ctypes.byref(d_q), ctypes.byref(d_k),
+                                          ctypes.byref(d_v), ctypes.byref(d_r), ctypes.byref(d_pt),
+                                          _ptr(row_offsets), _ptr(cache_lens), float(scale),
+                                          int(mask), _stream(stream)))
     return out
 
 

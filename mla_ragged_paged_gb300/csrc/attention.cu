@@ -31,6 +31,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -910,4 +911,56 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
   return MLA_OK;
+}
+
+// ------------------------------------------------------------ no-allocation entry point
+// Some callers cannot hand this library a workspace: a plug-in whose host
+// framework owns every byte of device memory through its own pool and offers
+// it no scratch buffer, or code on a latency-critical path where cudaMalloc
+// (which may synchronise the device) is not acceptable.  For them the
+// scheduler workspace lives in this fixed, file-scope device array instead,
+// sized for up to kNoAllocMaxBatch sequences (33,024 bytes).  Every GPU that
+// loads the library holds the array until the process exits.
+namespace mla {
+namespace {
+constexpr uint32_t kNoAllocMaxBatch = 1024;
+constexpr size_t kNoAllocBytes = sizeof(WsHeader) + kNoAllocMaxBatch * sizeof(SeqRec);
+static_assert(kNoAllocBytes % 256 == 0, "workspace size must keep 256-byte granularity");
+std::atomic<void*> g_noalloc_addr[64];
+}  // namespace
+}  // namespace mla
+
+static __device__ __align__(256) unsigned char g_noalloc_workspace[mla::kNoAllocBytes];
+
+extern "C" mla_status_t mla_prefill_ragged_noalloc(const mla_tensor_t* out, const mla_tensor_t* q,
+                                                   const mla_tensor_t* k_nope, const mla_tensor_t* v,
+                                                   const mla_tensor_t* k_rope_pages,
+                                                   const mla_tensor_t* page_table,
+                                                   const uint32_t* row_offsets,
+                                                   const uint32_t* cache_lens, float scale,
+                                                   mla_mask_t mask, mla_stream_t stream) {
+  using namespace mla;
+  if (!page_table) return fail(MLA_ERR_INVALID_ARG, "page_table descriptor is NULL");
+  if (page_table->shape[0] > static_cast<int64_t>(kNoAllocMaxBatch))
+    return fail(MLA_ERR_INVALID_ARG,
+                "batch %lld exceeds the %u sequences the built-in workspace of "
+                "mla_prefill_ragged_noalloc holds; use mla_prefill_ragged with a workspace",
+                (long long)page_table->shape[0], kNoAllocMaxBatch);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(MLA_ERR_UNSUPPORTED, "device index %d", dev);
+  // One-time set-up per device (the device is current here): the array's
+  // host-side name is only a stand-in, so ask the runtime for its address.
+  void* ws = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (!ws) {
+    e = cudaGetSymbolAddress(&ws, g_noalloc_workspace);
+    if (e != cudaSuccess || !ws)
+      return fail(MLA_ERR_CUDA, "cudaGetSymbolAddress(workspace): %s", cudaGetErrorString(e));
+    g_noalloc_addr[dev].store(ws, std::memory_order_release);
+  }
+  // The scheduler launch inside rewrites every workspace field the attention
+  // kernel reads (header, work counter, sequence records) on each call.
+  return mla_prefill_ragged(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,
+                            scale, mask, ws, kNoAllocBytes, stream);
 }
