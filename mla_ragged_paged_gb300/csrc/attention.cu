@@ -420,7 +420,7 @@ __device__ void mma_thread(Smem& s, uint32_t tmem, volatile uint32_t* abort) {
   const Ring ring{smem_u32(&s.kv_full[0]), smem_u32(&s.kv_empty[0]), smem_u32(&s.ring[0][0])};
   const uint32_t idS = make_idesc(128, 128, 1, false);
   const uint32_t idPV = make_idesc(128, 64, 1, true);
-  const uint32_t qbase[2] = {smem_u32(&s.q[0][0][0]), smem_u32(&s.q[1][0][0])};
+  const uint32_t q_smem0 = smem_u32(&s.q[0][0][0]);
   uint32_t pos = 0, item_k = 0, qf[2] = {0, 0}, pf[2] = {0, 0}, oe[2] = {0, 0};
   bool alive = true;
 
@@ -430,24 +430,29 @@ __device__ void mma_thread(Smem& s, uint32_t tmem, volatile uint32_t* abort) {
     tc_fence_after();
     return true;
   };
+  // S_q = Q_q . [K_nope | K_rope]^T: 3 swizzle atoms x 4 K-steps of 16.
   auto issue_s = [&](int q, uint32_t kpos) {
+    const uint64_t qd = sw128_desc_at(q_smem0 + static_cast<uint32_t>(q) * (3 * kChunk));
+    const uint32_t d = tmem + col_s(q);
 #pragma unroll
-    for (int ks = 0; ks < 12; ++ks) {
-      const int a = ks >> 2;
-      const uint32_t off = (ks & 3) * 32;
-      const uint64_t ad = sw128_desc(qbase[q] + a * kChunk + off, 16, 1024);
-      const uint64_t bd = sw128_desc(ring.buf(kpos + a) + off, 16, 1024);
-      umma_f16_ss(tmem + col_s(q), ad, bd, idS, ks > 0);
+    for (int a = 0; a < 3; ++a) {
+      const uint64_t kd = sw128_desc_at(ring.buf(kpos + a));
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        umma_f16_ss(d, qd + a * (kChunk >> 4) + 2 * k, kd + 2 * k, idS, (a | k) != 0);
     }
     umma_commit(smem_u32(&s.s_full[q]));
   };
+  // O_q (+)= P_q . V, P from TMEM; one N=64 UMMA per V chunk and K-step.
   auto issue_pv = [&](int q, uint32_t vpos, bool acc) {
-    const uint32_t v0 = ring.buf(vpos), v1 = ring.buf(vpos + 1);
+    const uint64_t v0 = sw128_desc_at(ring.buf(vpos)), v1 = sw128_desc_at(ring.buf(vpos + 1));
+    const uint32_t a0 = tmem + col_s(q), d = tmem + col_o(q);
+    const uint32_t acc0 = acc ? 1u : 0u;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t a = tmem + col_s(q) + ks * 8;
-      umma_f16_ts(tmem + col_o(q), a, sw128_desc(v0 + ks * 2048, 16, 1024), idPV, acc || ks > 0);
-      umma_f16_ts(tmem + col_o(q) + 64, a, sw128_desc(v1 + ks * 2048, 16, 1024), idPV, acc || ks > 0);
+      const uint32_t en = ks ? 1u : acc0;
+      umma_f16_ts(d, a0 + ks * 8, v0 + ks * (2048 >> 4), idPV, en);
+      umma_f16_ts(d + 64, a0 + ks * 8, v1 + ks * (2048 >> 4), idPV, en);
     }
   };
   auto release = [&](uint32_t first, int count) {
