@@ -1,5 +1,5 @@
 // Ragged causal MLA prefill attention for sm_103a (flare_mla_prefill:
-// description and Args).
+// description and Args; the k_rope_scales overload for fp8 inputs).
 //
 // Per work item (sequence b, head h, block of 256 query rows split into two
 // 128-row tiles Q0/Q1) one CTA streams the sequence's K context in 128-key
@@ -9,13 +9,13 @@
 //   O_q += P_q . V                           (UMMA, A = P read from TMEM)
 // The two Q tiles ping-pong so one tile's softmax overlaps the other tile's
 // GEMMs.  K_rope (64 dims shared by every head) is fetched from the paged
-// pool through the page table, one TMA box per page segment.
+// pool through the page table.
 //
 // Warp roles (384 threads = three warpgroups, one warp of each per SM
 // sub-partition):
 //   warp 0      producer: work-item fetch (atomic counter), TMA loads
 //   warp 1      UMMA issuer (one thread) and tensor-memory owner
-//   warps 2-3   idle
+//   warps 2-3   fp8 inputs only: K_rope / Q_rope conversion (else idle)
 //   warps 4-7   softmax + epilogue for Q0
 //   warps 8-11  softmax + epilogue for Q1
 // A warp may only touch TMEM lanes 32*(warp%4) .. +31, so each softmax
@@ -24,10 +24,18 @@
 // (setmaxnreg 120) so each softmax thread can hold its whole 128-column S row
 // (setmaxnreg 192): 120 + 2 * 192 = 3 * 168 per sub-partition.
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,384)
-// O1 [384,512); P_q is written as packed bf16 over the first 64 columns of S_q.
-// Shared memory: Q0/Q1 (3 x 16 KB each, 128B-swizzled K-major) and a ring of
-// eight 16 KB chunks carrying, per KV tile, K_nope[0:64], K_nope[64:128],
-// K_rope, V[:, 0:64], V[:, 64:128].
+// O1 [384,512); P_q is written over the first columns of S_q (packed bf16,
+// or four e4m3 per column for fp8 inputs).
+//
+// bf16 inputs: Q0/Q1 take 3 x 16 KB each (three 64-dim 128B-swizzled K-major
+// atoms); a ring of eight 16 KB chunks carries, per KV tile, K_nope[0:64],
+// K_nope[64:128], K_rope, V[:, 0:64], V[:, 64:128] (V MN-major).
+// fp8 inputs: Q_nope (e4m3, one 128-byte atom) and Q_rope (converted to bf16)
+// take 2 x 16 KB per tile; a ring of ten 16 KB chunks carries, per KV tile,
+// K_nope (e4m3), K_rope converted to bf16 as code * s_r[token] / s_k, and
+// V (e4m3, MN-major).  S = s_q s_k (q_nope . k_nope [e4m3 UMMA] + q_rope .
+// k_rope' [bf16 UMMA]) accumulates both parts in one fp32 tile; P is
+// quantised to e4m3 after a 2^6 prescale and P.V runs as an e4m3 UMMA.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -45,8 +53,6 @@ constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per KV tile
 constexpr int kQRows = 2 * kBM;   // query rows per work item
 constexpr int kChunk = 16384;     // 128 rows x 128 bytes
-constexpr int kRing = 8;
-constexpr int kChunksPerTile = 5;
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;  // registers per thread the register split assumes
 constexpr uint32_t kTmemCols = 512;
@@ -55,7 +61,19 @@ __device__ __forceinline__ uint32_t col_s(int q) { return q ? 128u : 0u; }
 __device__ __forceinline__ uint32_t col_o(int q) { return q ? 384u : 256u; }
 constexpr uint32_t kMaxBatch = 4096;
 constexpr uint64_t kL2GroupBytes = 32ull << 20;  // K/V bytes a head group should keep in L2
-constexpr float kRescaleThreshold = 8.0f;         // log2 units
+
+// Layout and numerics that depend on the input type.
+template <bool FP8>
+struct Cfg {
+  static constexpr int kQChunks = FP8 ? 2 : 3;   // 16 KB chunks per Q tile
+  static constexpr int kRing = FP8 ? 10 : 8;     // 16 KB ring slots
+  static constexpr int kCPT = FP8 ? 3 : 5;       // ring chunks per KV tile
+  // The running max used for the exponentials moves only when a tile's max
+  // exceeds it by more than this (log2 units); P <= 2^threshold.
+  static constexpr float kThreshold = FP8 ? 2.0f : 8.0f;
+  // fp8: P is stored as e4m3(p * 2^6) so that P <= 2^8 stays below 448.
+  static constexpr float kPScale = FP8 ? 64.0f : 1.0f;
+};
 
 struct WsHeader {
   uint32_t status;
@@ -90,14 +108,23 @@ struct AttnParams {
   uint32_t H, causal;
   float sl2;
   uint8_t* ws;
+  // fp8 inputs only.
+  const uint8_t* q_base;
+  long long q_tok, q_head;  // byte strides of q
+  uint32_t Tq;
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  const float* rope_scales;  // [num_pages * page_size]
 };
 
+template <bool FP8>
 struct __align__(1024) Smem {
-  uint8_t q[2][3][kChunk];
-  uint8_t ring[kRing][kChunk];
+  uint8_t q[2][Cfg<FP8>::kQChunks][kChunk];
+  uint8_t ring[Cfg<FP8>::kRing][kChunk];
   uint64_t item_full[2], item_empty[2];
   uint64_t q_full[2], q_empty[2];
-  uint64_t kv_full[kRing], kv_empty[kRing];
+  uint64_t kv_full[Cfg<FP8>::kRing], kv_empty[Cfg<FP8>::kRing];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t drain;
   ItemInfo items[2];
@@ -284,19 +311,42 @@ __device__ __forceinline__ ItemInfo decode_item(uint32_t t, const WsHeader* hdr,
   return it;
 }
 
+template <int R>
 struct Ring {
   uint32_t full, empty, data;  // shared addresses of kv_full[0], kv_empty[0], ring[0]
-  __device__ __forceinline__ uint32_t slot(uint32_t pos) const { return pos % kRing; }
-  __device__ __forceinline__ uint32_t phase(uint32_t pos) const { return (pos / kRing) & 1u; }
+  __device__ __forceinline__ uint32_t slot(uint32_t pos) const { return pos % R; }
+  __device__ __forceinline__ uint32_t phase(uint32_t pos) const { return (pos / R) & 1u; }
   __device__ __forceinline__ uint32_t full_bar(uint32_t pos) const { return full + 8u * slot(pos); }
   __device__ __forceinline__ uint32_t empty_bar(uint32_t pos) const { return empty + 8u * slot(pos); }
   __device__ __forceinline__ uint32_t buf(uint32_t pos) const { return data + kChunk * slot(pos); }
 };
 
-__device__ void producer_warp(Smem& s, const AttnParams& p, int lane, volatile uint32_t* abort) {
+template <bool FP8>
+__device__ __forceinline__ Ring<Cfg<FP8>::kRing> make_ring(Smem<FP8>& s) {
+  return Ring<Cfg<FP8>::kRing>{smem_u32(&s.kv_full[0]), smem_u32(&s.kv_empty[0]),
+                               smem_u32(&s.ring[0][0])};
+}
+
+// Reads the next work item from the item ring (every consumer warp reads
+// every item; lane 0 releases the slot after the whole warp has read it).
+template <bool FP8>
+__device__ __forceinline__ bool read_item(Smem<FP8>& s, uint32_t& item_k, int lane, ItemInfo& it,
+                                          volatile uint32_t* abort) {
+  const uint32_t islot = item_k & 1u;
+  if (!mbar_wait(smem_u32(&s.item_full[islot]), (item_k >> 1) & 1u, abort)) return false;
+  it = s.items[islot];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&s.item_empty[islot]));
+  ++item_k;
+  return true;
+}
+
+template <bool FP8>
+__device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volatile uint32_t* abort) {
+  using C = Cfg<FP8>;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
   const SeqRec* recs = reinterpret_cast<const SeqRec*>(p.ws + sizeof(WsHeader));
-  const Ring ring{smem_u32(&s.kv_full[0]), smem_u32(&s.kv_empty[0]), smem_u32(&s.ring[0][0])};
+  const auto ring = make_ring(s);
   uint32_t pos = 0, item_k = 0, q_uses[2] = {0, 0};
   uint32_t status = 0;
   bool alive = true;
@@ -304,10 +354,12 @@ __device__ void producer_warp(Smem& s, const AttnParams& p, int lane, volatile u
   auto acquire = [&](uint32_t ps) -> bool {
     return mbar_wait(ring.empty_bar(ps), ring.phase(ps) ^ 1u, abort);
   };
-  auto load_nope = [&](const CUtensorMap* map, int x, const ItemInfo& it, int j) -> bool {
+  // One 16 KB TMA box (128 rows) of k_nope or v into the next ring slot.
+  auto load_chunk = [&](const CUtensorMap* map, int x, const ItemInfo& it, int j) -> bool {
     if (!acquire(pos)) return false;
     if (lane == 0) {
       mbar_arrive_expect_tx(ring.full_bar(pos), kChunk);
+      if (FP8) mbar_arrive(ring.full_bar(pos));  // fp8 slots count two arrivals
       tma_load_3d(ring.buf(pos), map, ring.full_bar(pos), x, it.h, it.kv_row0 + j * kBN);
     }
     ++pos;
@@ -374,13 +426,15 @@ __device__ void producer_warp(Smem& s, const AttnParams& p, int lane, volatile u
     ++pos;
     return true;
   };
+  // bf16: the whole 192-wide Q tile (three 64-dim atoms).  fp8: the 128
+  // nope codes only; the converter warps write the rope part.
   auto load_q = [&](int q, const ItemInfo& it) -> bool {
     const uint32_t bar = smem_u32(&s.q_full[q]);
     if (!mbar_wait(smem_u32(&s.q_empty[q]), (q_uses[q] & 1u) ^ 1u, abort)) return false;
     ++q_uses[q];
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar, 3 * kChunk);
-      for (int a = 0; a < 3; ++a)
+      mbar_arrive_expect_tx(bar, (FP8 ? 1 : 3) * kChunk);
+      for (int a = 0; a < (FP8 ? 1 : 3); ++a)
         tma_load_3d(smem_u32(&s.q[q][a][0]), &p.tm_q, bar, 64 * a, it.h, it.q_row0 + q * kBM);
     }
     return true;
@@ -401,25 +455,138 @@ __device__ void producer_warp(Smem& s, const AttnParams& p, int lane, volatile u
     if (!it.valid) break;
     const int nkv = it.n1 > 0 ? it.nkv1 : it.nkv0;
     for (int j = 0; j < nkv && alive; ++j) {
-      alive = load_nope(&p.tm_k, 0, it, j) && load_nope(&p.tm_k, 64, it, j) && load_rope(it, j);
+      if (FP8) {
+        alive = load_chunk(&p.tm_k, 0, it, j);
+        ++pos;  // the converter warps fill the K_rope slot
+      } else {
+        alive = load_chunk(&p.tm_k, 0, it, j) && load_chunk(&p.tm_k, 64, it, j) && load_rope(it, j);
+      }
       if (alive && j == 0) alive = load_q(0, it) && (it.n1 == 0 || load_q(1, it));
-      alive = alive && load_nope(&p.tm_v, 0, it, j) && load_nope(&p.tm_v, 64, it, j);
+      if (FP8) alive = alive && load_chunk(&p.tm_v, 0, it, j);
+      else alive = alive && load_chunk(&p.tm_v, 0, it, j) && load_chunk(&p.tm_v, 64, it, j);
     }
   }
   if (status) atomicOr(&hdr->status, status);
   if (*abort) {
     // Let every copy this warp started land before the CTA exits.
-    for (uint32_t ps = pos > kRing ? pos - kRing : 0; ps < pos; ++ps)
-      wait_drain(ring.full_bar(ps), ring.phase(ps));
+    for (uint32_t ps = pos > C::kRing ? pos - C::kRing : 0; ps < pos; ++ps)
+      if (!FP8 || ps % C::kCPT != 1) wait_drain(ring.full_bar(ps), ring.phase(ps));
     for (int q = 0; q < 2; ++q)
       if (q_uses[q]) wait_drain(smem_u32(&s.q_full[q]), (q_uses[q] - 1) & 1u);
   }
 }
 
-__device__ void mma_thread(Smem& s, uint32_t tmem, volatile uint32_t* abort) {
-  const Ring ring{smem_u32(&s.kv_full[0]), smem_u32(&s.kv_empty[0]), smem_u32(&s.ring[0][0])};
-  const uint32_t idS = make_idesc(128, 128, 1, false);
-  const uint32_t idPV = make_idesc(128, 64, 1, true);
+// fp8 inputs: warps 2 and 3 turn the rope parts into bf16 UMMA operands.
+//   Q_rope:  64 e4m3 codes per query row -> bf16 (exact), 128B-swizzled.
+//   K_rope:  per key, the paged pool row (64 codes) times s_r[slot] / s_k,
+//            rounded to bf16, so that q_rope . k_rope' shares the s_q s_k
+//            factor of the nope part.
+// Each lane owns two of the 128 rows; each warp signals the slot's mbarrier
+// once its rows are written (kv_full / q_full count both warps).
+__device__ __forceinline__ void store_bf16_row(uint32_t dst, int r, const float (&f)[64]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t a = dst + r * 128 + ((c ^ (r & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                 "r"(pack_bf16x2(f[8 * c], f[8 * c + 1])), "r"(pack_bf16x2(f[8 * c + 2], f[8 * c + 3])),
+                 "r"(pack_bf16x2(f[8 * c + 4], f[8 * c + 5])), "r"(pack_bf16x2(f[8 * c + 6], f[8 * c + 7]))
+                 : "memory");
+  }
+}
+__device__ __forceinline__ void load_e4m3_row(const uint8_t* src, float scale, float (&f)[64]) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 v = s4[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float a, b, cc, d;
+      e4m3x4_to_f32(w[e], a, b, cc, d);
+      f[16 * c + 4 * e] = a * scale;
+      f[16 * c + 4 * e + 1] = b * scale;
+      f[16 * c + 4 * e + 2] = cc * scale;
+      f[16 * c + 4 * e + 3] = d * scale;
+    }
+  }
+}
+__device__ void converter_warps(Smem<true>& s, const AttnParams& p, int cl, volatile uint32_t* abort) {
+  using C = Cfg<true>;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
+  const auto ring = make_ring(s);
+  const int lane = cl & 31;
+  const float inv_sk = 1.f / *p.k_scale;
+  uint32_t pos = 0, item_k = 0, q_uses[2] = {0, 0}, status = 0;
+  bool alive = true;
+
+  auto signal = [&](uint32_t bar) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+  };
+  auto conv_q = [&](int q, const ItemInfo& it) -> bool {
+    if (!mbar_wait(smem_u32(&s.q_empty[q]), (q_uses[q] & 1u) ^ 1u, abort)) return false;
+    ++q_uses[q];
+    const uint32_t dst = smem_u32(&s.q[q][1][0]);
+    for (int r = cl; r < kBM; r += 64) {
+      const int row = it.q_row0 + q * kBM + r;
+      float f[64];
+      if (row < static_cast<int>(p.Tq)) {
+        load_e4m3_row(p.q_base + row * p.q_tok + it.h * p.q_head + 128, 1.f, f);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) f[e] = 0.f;
+      }
+      store_bf16_row(dst, r, f);
+    }
+    signal(smem_u32(&s.q_full[q]));
+    return true;
+  };
+  auto conv_rope = [&](const ItemInfo& it, int j) -> bool {
+    if (!mbar_wait(ring.empty_bar(pos), ring.phase(pos) ^ 1u, abort)) return false;
+    const uint32_t dst = ring.buf(pos);
+    for (int r = cl; r < kBN; r += 64) {
+      const int key = j * kBN + r;
+      if (key >= it.L) continue;  // masked keys: stale data is never used
+      const uint32_t col = static_cast<uint32_t>(key) / p.page_size;
+      if (col >= p.max_pages) { status |= MLA_DEVICE_STATUS_BAD_COLUMN; continue; }
+      const uint32_t page = p.page_table[static_cast<long long>(it.b) * p.pt_stride + col];
+      if (page >= p.num_pages) { status |= MLA_DEVICE_STATUS_BAD_PAGE; continue; }
+      const uint32_t in_page = static_cast<uint32_t>(key) - col * p.page_size;
+      const float sc = p.rope_scales[static_cast<long long>(page) * p.page_size + in_page] * inv_sk;
+      float f[64];
+      load_e4m3_row(p.rope_base + page * p.rope_page_bytes + in_page * p.rope_tok_bytes, sc, f);
+      store_bf16_row(dst, r, f);
+    }
+    signal(ring.full_bar(pos));
+    ++pos;
+    return true;
+  };
+
+  while (alive) {
+    ItemInfo it;
+    if (!read_item(s, item_k, lane, it, abort) || !it.valid) break;
+    const int nkv = it.n1 > 0 ? it.nkv1 : it.nkv0;
+    for (int j = 0; j < nkv && alive; ++j) {
+      pos += 1;  // K_nope slot (producer)
+      alive = conv_rope(it, j);
+      if (alive && j == 0) alive = conv_q(0, it) && (it.n1 == 0 || conv_q(1, it));
+      pos += 1;  // V slot (producer)
+    }
+    (void)C::kCPT;
+  }
+  if (status) atomicOr(&hdr->status, status);
+}
+
+template <bool FP8>
+__device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort) {
+  using C = Cfg<FP8>;
+  const auto ring = make_ring(s);
+  // Instruction descriptors (fp32 accumulate): bf16 A/B (format 1) or e4m3 (format 0).
+  const uint32_t idS = make_idesc(128, 128, 1, false);     // bf16 S (whole S, or fp8's rope part)
+  const uint32_t idS8 = make_idesc(128, 128, 0, false);    // fp8 nope part of S
+  const uint32_t idPV = make_idesc(128, 64, 1, true);      // bf16 P.V, N = 64 per V chunk
+  const uint32_t idPV8 = make_idesc(128, 128, 0, true);    // fp8 P.V, N = 128
   const uint32_t q_smem0 = smem_u32(&s.q[0][0][0]);
   uint32_t pos = 0, item_k = 0, qf[2] = {0, 0}, pf[2] = {0, 0}, oe[2] = {0, 0};
   bool alive = true;
@@ -430,29 +597,49 @@ __device__ void mma_thread(Smem& s, uint32_t tmem, volatile uint32_t* abort) {
     tc_fence_after();
     return true;
   };
-  // S_q = Q_q . [K_nope | K_rope]^T: 3 swizzle atoms x 4 K-steps of 16.
+  // S_q = Q_q . [K_nope | K_rope]^T.
   auto issue_s = [&](int q, uint32_t kpos) {
-    const uint64_t qd = sw128_desc_at(q_smem0 + static_cast<uint32_t>(q) * (3 * kChunk));
+    const uint64_t qd = sw128_desc_at(q_smem0 + static_cast<uint32_t>(q) * (C::kQChunks * kChunk));
     const uint32_t d = tmem + col_s(q);
+    if (FP8) {
+      // 4 e4m3 K-steps of 32 over the nope atom, then 4 bf16 K-steps of 16 over rope.
+      const uint64_t kd = sw128_desc_at(ring.buf(kpos)), rd = sw128_desc_at(ring.buf(kpos + 1));
 #pragma unroll
-    for (int a = 0; a < 3; ++a) {
-      const uint64_t kd = sw128_desc_at(ring.buf(kpos + a));
+      for (int k = 0; k < 4; ++k) umma_f8_ss(d, qd + 2 * k, kd + 2 * k, idS8, k != 0);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        umma_f16_ss(d, qd + a * (kChunk >> 4) + 2 * k, kd + 2 * k, idS, (a | k) != 0);
+        umma_f16_ss(d, qd + (kChunk >> 4) + 2 * k, rd + 2 * k, idS, 1);
+    } else {
+      // 3 swizzle atoms x 4 K-steps of 16.
+#pragma unroll
+      for (int a = 0; a < 3; ++a) {
+        const uint64_t kd = sw128_desc_at(ring.buf(kpos + a));
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_f16_ss(d, qd + a * (kChunk >> 4) + 2 * k, kd + 2 * k, idS, (a | k) != 0);
+      }
     }
     umma_commit(smem_u32(&s.s_full[q]));
   };
-  // O_q (+)= P_q . V, P from TMEM; one N=64 UMMA per V chunk and K-step.
+  // O_q (+)= P_q . V, P from TMEM.
   auto issue_pv = [&](int q, uint32_t vpos, bool acc) {
-    const uint64_t v0 = sw128_desc_at(ring.buf(vpos)), v1 = sw128_desc_at(ring.buf(vpos + 1));
     const uint32_t a0 = tmem + col_s(q), d = tmem + col_o(q);
     const uint32_t acc0 = acc ? 1u : 0u;
+    if (FP8) {
+      // 4 K-steps of 32 keys; P holds four e4m3 per column, V is one MN-major atom.
+      const uint64_t v0 = sw128_desc_at(ring.buf(vpos));
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t en = ks ? 1u : acc0;
-      umma_f16_ts(d, a0 + ks * 8, v0 + ks * (2048 >> 4), idPV, en);
-      umma_f16_ts(d + 64, a0 + ks * 8, v1 + ks * (2048 >> 4), idPV, en);
+      for (int ks = 0; ks < 4; ++ks)
+        umma_f8_ts(d, a0 + ks * 8, v0 + ks * (4096 >> 4), idPV8, ks ? 1u : acc0);
+    } else {
+      // one N=64 UMMA per V chunk and K-step of 16 keys.
+      const uint64_t v0 = sw128_desc_at(ring.buf(vpos)), v1 = sw128_desc_at(ring.buf(vpos + 1));
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t en = ks ? 1u : acc0;
+        umma_f16_ts(d, a0 + ks * 8, v0 + ks * (2048 >> 4), idPV, en);
+        umma_f16_ts(d + 64, a0 + ks * 8, v1 + ks * (2048 >> 4), idPV, en);
+      }
     }
   };
   auto release = [&](uint32_t first, int count) {
@@ -468,6 +655,8 @@ __device__ void mma_thread(Smem& s, uint32_t tmem, volatile uint32_t* abort) {
     tc_fence_after();
     return true;
   };
+  constexpr int kK = FP8 ? 2 : 3;  // K chunks per tile (ring order: K chunks, then V chunks)
+  constexpr int kV = C::kCPT - kK;
 
   while (alive) {
     const uint32_t islot = item_k & 1u;
@@ -478,9 +667,8 @@ __device__ void mma_thread(Smem& s, uint32_t tmem, volatile uint32_t* abort) {
     if (!it.valid) break;
     const bool has1 = it.n1 > 0;
     const int nkv = has1 ? it.nkv1 : it.nkv0;
-    // Per tile j: K chunks at pos + 5j .. +2, V chunks at pos + 5j + 3 .. +4.
-    auto kpos = [&](int j) { return pos + kChunksPerTile * j; };
-    alive = wait_chunks(kpos(0), 3);
+    auto kpos = [&](int j) { return pos + C::kCPT * j; };
+    alive = wait_chunks(kpos(0), kK);
     alive = alive && mbar_wait(smem_u32(&s.q_full[0]), qf[0] & 1u, abort);
     ++qf[0];
     if (alive && has1) {
@@ -491,7 +679,7 @@ __device__ void mma_thread(Smem& s, uint32_t tmem, volatile uint32_t* abort) {
     tc_fence_after();
     issue_s(0, kpos(0));
     if (has1) issue_s(1, kpos(0));
-    release(kpos(0), 3);
+    release(kpos(0), kK);
     for (int j = 0; j < nkv && alive; ++j) {
       const bool on0 = j < it.nkv0;
       const bool next0 = j + 1 < it.nkv0;
@@ -500,12 +688,12 @@ __device__ void mma_thread(Smem& s, uint32_t tmem, volatile uint32_t* abort) {
       auto need_k_next = [&]() -> bool {
         if (k_next) return true;
         k_next = true;
-        return wait_chunks(kpos(j + 1), 3);
+        return wait_chunks(kpos(j + 1), kK);
       };
-      if (!(alive = wait_chunks(kpos(j) + 3, 2))) break;
+      if (!(alive = wait_chunks(kpos(j) + kK, kV))) break;
       if (on0) {
         if (!(alive = wait_p(0, j == 0))) break;
-        issue_pv(0, kpos(j) + 3, j > 0);
+        issue_pv(0, kpos(j) + kK, j > 0);
         if (next0) {
           if (!(alive = need_k_next())) break;
           issue_s(0, kpos(j + 1));
@@ -516,8 +704,8 @@ __device__ void mma_thread(Smem& s, uint32_t tmem, volatile uint32_t* abort) {
       }
       if (has1) {
         if (!(alive = wait_p(1, j == 0))) break;
-        issue_pv(1, kpos(j) + 3, j > 0);
-        release(kpos(j) + 3, 2);
+        issue_pv(1, kpos(j) + kK, j > 0);
+        release(kpos(j) + kK, kV);
         if (next1) {
           if (!(alive = need_k_next())) break;
           issue_s(1, kpos(j + 1));
@@ -526,35 +714,34 @@ __device__ void mma_thread(Smem& s, uint32_t tmem, volatile uint32_t* abort) {
           umma_commit(smem_u32(&s.q_empty[1]));
         }
       } else {
-        release(kpos(j) + 3, 2);
+        release(kpos(j) + kK, kV);
       }
-      if (next0 || next1) release(kpos(j + 1), 3);
+      if (next0 || next1) release(kpos(j + 1), kK);
     }
-    pos += kChunksPerTile * nkv;
+    pos += C::kCPT * nkv;
   }
   // Make sure no UMMA is still in flight before tensor memory is released.
   umma_commit(smem_u32(&s.drain));
   wait_drain(smem_u32(&s.drain), 0);
 }
 
-__device__ void softmax_warp(Smem& s, const AttnParams& p, uint32_t tmem, int q, int wq, int lane,
-                             volatile uint32_t* abort) {
+template <bool FP8>
+__device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, int q, int wq,
+                             int lane, volatile uint32_t* abort) {
+  using C = Cfg<FP8>;
   const int r = wq * 32 + lane;  // query row inside the tile == TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t t_s = tmem + lane_off + col_s(q);
   const uint32_t t_o = tmem + lane_off + col_o(q);
-  const float sl2 = p.sl2;
+  // fp8: S in TMEM is in units of s_q * s_k; O in units of s_v * kPScale.
+  const float sl2 = FP8 ? p.sl2 * (*p.q_scale) * (*p.k_scale) : p.sl2;
+  const float out_scale = FP8 ? (*p.v_scale) / C::kPScale : 1.f;
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
   uint32_t item_k = 0, sf = 0, of = 0;
 
   for (;;) {
-    const uint32_t islot = item_k & 1u;
-    if (!mbar_wait(smem_u32(&s.item_full[islot]), (item_k >> 1) & 1u, abort)) return;
-    const ItemInfo it = s.items[islot];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&s.item_empty[islot]));
-    ++item_k;
-    if (!it.valid) return;
+    ItemInfo it;
+    if (!read_item(s, item_k, lane, it, abort) || !it.valid) return;
     if (q == 1 && it.n1 == 0) continue;
     const int nkv = q ? it.nkv1 : it.nkv0;
     const int i = it.i0 + q * kBM + r;  // query index inside the sequence
@@ -590,7 +777,7 @@ __device__ void softmax_warp(Smem& s, const AttnParams& p, uint32_t tmem, int q,
           smax = max3(smax, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
       const float m_tile = smax == -INFINITY ? -INFINITY : smax * sl2;
       const float m_new = fmaxf(m_used, m_tile);
-      const bool grow = m_new > m_used + kRescaleThreshold;
+      const bool grow = m_new > m_used + C::kThreshold;
       float alpha = 1.f;
       if (grow) {
         alpha = ex2_approx(m_used - m_new);
@@ -614,11 +801,23 @@ __device__ void softmax_warp(Smem& s, const AttnParams& p, uint32_t tmem, int q,
             p0 = col < nvalid ? p0 : 0.f;
             p1 = col + 1 < nvalid ? p1 : 0.f;
           }
-          const uint64_t pp = f2_pack(p0, p1);
-          lacc = f2_add(lacc, pp);
-          pk[e] = pack_bf16x2(p0, p1);
+          lacc = f2_add(lacc, f2_pack(p0, p1));
+          if (FP8) {
+            // 4 codes per column: pairs e (even) and e+1 (odd) share one word.
+            const uint32_t two = pack_e4m3x2(p0 * C::kPScale, p1 * C::kPScale);
+            pk[e >> 1] = (e & 1) ? (pk[e >> 1] | (two << 16)) : two;
+          } else {
+            pk[e] = pack_bf16x2(p0, p1);
+          }
         }
-        tmem_st_32x32b_x16(t_s + 16 * c, pk);
+        if (FP8) {
+          uint32_t w8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w8[e] = pk[e];
+          tmem_st_32x32b_x8(t_s + 8 * c, w8);
+        } else {
+          tmem_st_32x32b_x16(t_s + 16 * c, pk);
+        }
       }
       float l0, l1;
       f2_unpack(lacc, l0, l1);
@@ -652,7 +851,7 @@ __device__ void softmax_warp(Smem& s, const AttnParams& p, uint32_t tmem, int q,
     if (!mbar_wait(smem_u32(&s.o_full[q]), of & 1u, abort)) return;
     ++of;
     tc_fence_after();
-    const float inv = 1.f / l;
+    const float inv = out_scale / l;
     const uint64_t inv2 = f2_pack(inv, inv);
     const bool store = i < it.n;
     uint4* dst = reinterpret_cast<uint4*>(
@@ -682,9 +881,12 @@ __device__ void softmax_warp(Smem& s, const AttnParams& p, uint32_t tmem, int q,
   }
 }
 
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid_constant__ AttnParams p) {
+  using C = Cfg<FP8>;
   extern __shared__ uint8_t smem_raw[];
-  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem<FP8>& s =
+      *reinterpret_cast<Smem<FP8>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile uint32_t* abort = &s.abort_flag;
 
@@ -692,16 +894,19 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
     s.abort_flag = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.item_full[i]), 1);
-      mbar_init(smem_u32(&s.item_empty[i]), 9);  // MMA thread + 8 softmax warps
-      mbar_init(smem_u32(&s.q_full[i]), 1);
+      // MMA thread + 8 softmax warps (+ 2 converter warps for fp8)
+      mbar_init(smem_u32(&s.item_empty[i]), FP8 ? 11 : 9);
+      mbar_init(smem_u32(&s.q_full[i]), FP8 ? 3 : 1);  // TMA (+ two rope converter warps)
       mbar_init(smem_u32(&s.q_empty[i]), 1);
       mbar_init(smem_u32(&s.s_full[i]), 1);
       mbar_init(smem_u32(&s.p_full[i]), 4);
       mbar_init(smem_u32(&s.o_full[i]), 1);
       mbar_init(smem_u32(&s.o_empty[i]), 4);
     }
-    for (int i = 0; i < kRing; ++i) {
-      mbar_init(smem_u32(&s.kv_full[i]), 1);
+    for (int i = 0; i < C::kRing; ++i) {
+      // fp8: a K_rope slot is filled by two converter warps, so every slot
+      // takes two arrivals (the producer arrives twice on its own slots).
+      mbar_init(smem_u32(&s.kv_full[i]), FP8 ? 2 : 1);
       mbar_init(smem_u32(&s.kv_empty[i]), 1);
     }
     mbar_init(smem_u32(&s.drain), 1);
@@ -711,7 +916,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
-    if (!p.rope_manual) tma_prefetch_desc(&p.tm_rope);
+    if (!FP8 && !p.rope_manual) tma_prefetch_desc(&p.tm_rope);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&s.tmem_base), kTmemCols);
@@ -725,14 +930,16 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
     if (warp == 0) {
-      producer_warp(s, p, lane, abort);
+      producer_warp<FP8>(s, p, lane, abort);
     } else if (warp == 1) {
-      if (lane == 0) mma_thread(s, tmem, abort);
+      if (lane == 0) mma_thread<FP8>(s, tmem, abort);
       __syncwarp();
+    } else if constexpr (FP8) {
+      converter_warps(s, p, threadIdx.x - 64, abort);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
-    softmax_warp(s, p, tmem, (warp - 4) >> 2, warp & 3, lane, abort);
+    softmax_warp<FP8>(s, p, tmem, (warp - 4) >> 2, warp & 3, lane, abort);
   }
 
   tc_fence_before();
@@ -770,6 +977,52 @@ extern "C" size_t mla_prefill_ragged_workspace_size(uint32_t batch) {
   return (bytes + 255) & ~size_t(255);
 }
 
+namespace mla {
+namespace {
+
+// Launches the scheduler and the attention kernel for one input type.
+template <bool FP8>
+mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t* row_offsets,
+                              const uint32_t* cache_lens, uint32_t B, uint32_t H, uint32_t Tq,
+                              uint32_t Sk, uint32_t P, uint32_t max_pages, void* workspace,
+                              cudaStream_t cs) {
+  mla_status_t st;
+  auto* kernel = mla_attention_kernel<FP8>;
+  {
+    // The register split inside the kernel is only safe when the kernel was
+    // built with exactly kLaunchRegs registers per thread.
+    static int checked[64] = {0};
+    if (dev < 64 && !checked[dev]) {
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+      if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
+      if (fa.numRegs != kLaunchRegs)
+        return fail(MLA_ERR_UNSUPPORTED, "attention kernel built with %d registers per thread, expected %d",
+                    fa.numRegs, kLaunchRegs);
+      checked[dev] = 1;
+    }
+  }
+  const int sched_smem = static_cast<int>(3 * B * sizeof(uint32_t));
+  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(schedule_kernel), sched_smem, dev, 1)) != MLA_OK)
+    return st;
+  const int attn_smem = static_cast<int>(sizeof(Smem<FP8>) + 1024);
+  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), attn_smem, dev, FP8 ? 3 : 2)) != MLA_OK)
+    return st;
+  const uint32_t elt = FP8 ? 1u : 2u;
+  schedule_kernel<<<1, kSchedThreads, sched_smem, cs>>>(row_offsets, cache_lens, B, H, Tq, Sk, P,
+                                                        max_pages, elt * (128 + 128),
+                                                        static_cast<uint8_t*>(workspace));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "scheduler launch: %s", cudaGetErrorString(e));
+  kernel<<<sms, kThreads, attn_smem, cs>>>(prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  return MLA_OK;
+}
+
+}  // namespace
+}  // namespace mla
+
 extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_tensor_t* q,
                                            const mla_tensor_t* k_nope, const mla_tensor_t* v,
                                            const mla_tensor_t* k_rope_pages,
@@ -780,15 +1033,23 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
   using namespace mla;
   mla_status_t st;
   if (!q) return fail(MLA_ERR_INVALID_ARG, "q descriptor is NULL");
-  if (q->dtype == MLA_DTYPE_FP8_E4M3)
-    return fail(MLA_ERR_UNSUPPORTED, "fp8 inputs are not built into this library version");
-  const mla_dtype_t dt = MLA_DTYPE_BF16;
+  const bool fp8 = q->dtype == MLA_DTYPE_FP8_E4M3;
+  const mla_dtype_t dt = fp8 ? MLA_DTYPE_FP8_E4M3 : MLA_DTYPE_BF16;
   if ((st = check_tensor(q, "q", 3, dt)) != MLA_OK) return st;
   if ((st = check_tensor(out, "out", 3, MLA_DTYPE_BF16)) != MLA_OK) return st;
   if ((st = check_tensor(k_nope, "k_nope", 3, dt)) != MLA_OK) return st;
   if ((st = check_tensor(v, "v", 3, dt)) != MLA_OK) return st;
   if ((st = check_tensor(k_rope_pages, "k_rope_pages", 3, dt)) != MLA_OK) return st;
   if ((st = check_tensor(page_table, "page_table", 2, MLA_DTYPE_U32)) != MLA_OK) return st;
+  if (fp8) {
+    const mla_tensor_t* pt[3] = {q, k_nope, v};
+    const char* pn[3] = {"q", "k_nope", "v"};
+    for (int i = 0; i < 3; ++i)
+      if (!pt[i]->scale || pt[i]->scale_gran != MLA_SCALE_PER_TENSOR)
+        return fail(MLA_ERR_INVALID_ARG, "fp8 %s needs a per-tensor scale", pn[i]);
+    if (!k_rope_pages->scale || k_rope_pages->scale_gran != MLA_SCALE_PER_TOKEN)
+      return fail(MLA_ERR_INVALID_ARG, "fp8 k_rope_pages needs per-token scales");
+  }
   if (!row_offsets || !cache_lens) return fail(MLA_ERR_INVALID_ARG, "row_offsets / cache_lens is NULL");
   if (mask != MLA_MASK_CAUSAL && mask != MLA_MASK_NULL) return fail(MLA_ERR_INVALID_ARG, "unknown mask %d", (int)mask);
   if (!(scale >= 0.f) || !std::isfinite(scale)) return fail(MLA_ERR_INVALID_ARG, "scale must be finite and >= 0");
@@ -813,14 +1074,15 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
     return fail(MLA_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
   if (workspace_bytes < mla_prefill_ragged_workspace_size(static_cast<uint32_t>(B)))
     return fail(MLA_ERR_INVALID_ARG, "workspace too small");
-  // TMA and vector-store constraints: 16-byte aligned bases and strides.
+  // TMA and vector-access constraints: 16-byte aligned bases and strides.
   const mla_tensor_t* ts[5] = {q, k_nope, v, k_rope_pages, out};
   const char* names[5] = {"q", "k_nope", "v", "k_rope_pages", "out"};
   for (int i = 0; i < 5; ++i) {
+    const int64_t es = (i < 4 && fp8) ? 1 : 2;
     if (!aligned16(ts[i]->data)) return fail(MLA_ERR_INVALID_ARG, "%s data must be 16-byte aligned", names[i]);
     for (int d = 0; d < 2; ++d)
-      if ((ts[i]->stride[d] * 2) % 16 != 0 || ts[i]->stride[d] * 2 >= (1ll << 40))
-        return fail(MLA_ERR_INVALID_ARG, "%s stride[%d] must be a multiple of 8 elements", names[i], d);
+      if ((ts[i]->stride[d] * es) % 16 != 0 || ts[i]->stride[d] * es >= (1ll << 40))
+        return fail(MLA_ERR_INVALID_ARG, "%s stride[%d] must be a multiple of 16 bytes", names[i], d);
   }
 
   int dev = 0, sms = 0;
@@ -834,24 +1096,26 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
 
   AttnParams prm;
   memset(&prm, 0, sizeof(prm));
+  const int64_t es = fp8 ? 1 : 2;
+  const CUtensorMapDataType tdt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  // Boxes are 128 bytes wide (one swizzle atom): 64 bf16 or 128 e4m3 codes.
+  const uint32_t inner = fp8 ? 128 : 64;
   {
     uint64_t dims[3] = {192, (uint64_t)H, (uint64_t)Tq};
-    uint64_t str[2] = {(uint64_t)q->stride[1] * 2, (uint64_t)q->stride[0] * 2};
-    uint32_t box[3] = {64, 1, kBM};
-    if ((st = encode_tiled(&prm.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q->data, dims, str, box,
-                           CU_TENSOR_MAP_SWIZZLE_128B, "q")) != MLA_OK)
+    uint64_t str[2] = {(uint64_t)(q->stride[1] * es), (uint64_t)(q->stride[0] * es)};
+    uint32_t box[3] = {inner, 1, kBM};
+    if ((st = encode_tiled(&prm.tm_q, tdt, 3, q->data, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B, "q")) != MLA_OK)
       return st;
   }
   {
     uint64_t dims[3] = {128, (uint64_t)H, (uint64_t)Sk};
-    uint32_t box[3] = {64, 1, kBN};
-    uint64_t str[2] = {(uint64_t)k_nope->stride[1] * 2, (uint64_t)k_nope->stride[0] * 2};
-    if ((st = encode_tiled(&prm.tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_nope->data, dims, str, box,
-                           CU_TENSOR_MAP_SWIZZLE_128B, "k_nope")) != MLA_OK)
+    uint32_t box[3] = {inner, 1, kBN};
+    uint64_t str[2] = {(uint64_t)(k_nope->stride[1] * es), (uint64_t)(k_nope->stride[0] * es)};
+    if ((st = encode_tiled(&prm.tm_k, tdt, 3, k_nope->data, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                           "k_nope")) != MLA_OK)
       return st;
-    uint64_t strv[2] = {(uint64_t)v->stride[1] * 2, (uint64_t)v->stride[0] * 2};
-    if ((st = encode_tiled(&prm.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v->data, dims, strv, box,
-                           CU_TENSOR_MAP_SWIZZLE_128B, "v")) != MLA_OK)
+    uint64_t strv[2] = {(uint64_t)(v->stride[1] * es), (uint64_t)(v->stride[0] * es)};
+    if ((st = encode_tiled(&prm.tm_v, tdt, 3, v->data, dims, strv, box, CU_TENSOR_MAP_SWIZZLE_128B, "v")) != MLA_OK)
       return st;
   }
   uint32_t g = 1;
@@ -860,7 +1124,7 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
     while (b) { uint32_t t = a % b; a = b; b = t; }
     g = a;  // gcd(P, 128): rows per page segment inside a key tile
   }
-  prm.rope_manual = (g % 8u) != 0;
+  prm.rope_manual = fp8 || (g % 8u) != 0;
   prm.rope_box = g;
   if (!prm.rope_manual) {
     uint64_t dims[3] = {64, (uint64_t)P, (uint64_t)NP};
@@ -876,8 +1140,8 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
   prm.page_table = static_cast<const uint32_t*>(page_table->data);
   prm.pt_stride = page_table->stride[0];
   prm.rope_base = static_cast<const uint8_t*>(k_rope_pages->data);
-  prm.rope_tok_bytes = k_rope_pages->stride[1] * 2;
-  prm.rope_page_bytes = k_rope_pages->stride[0] * 2;
+  prm.rope_tok_bytes = k_rope_pages->stride[1] * es;
+  prm.rope_page_bytes = k_rope_pages->stride[0] * es;
   prm.max_pages = static_cast<uint32_t>(max_pages);
   prm.num_pages = static_cast<uint32_t>(NP);
   prm.page_size = static_cast<uint32_t>(P);
@@ -885,37 +1149,20 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
   prm.causal = mask == MLA_MASK_CAUSAL;
   prm.sl2 = scale * 1.4426950408889634f;
   prm.ws = static_cast<uint8_t*>(workspace);
-
-  const int sched_smem = static_cast<int>(3 * B * sizeof(uint32_t));
-  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(schedule_kernel), sched_smem, dev, 1)) != MLA_OK)
-    return st;
-  {
-    // The register split inside the kernel is only safe when the kernel was
-    // built with exactly kLaunchRegs registers per thread.
-    static int checked[64] = {0};
-    if (dev < 64 && !checked[dev]) {
-      cudaFuncAttributes fa;
-      cudaError_t e = cudaFuncGetAttributes(&fa, mla_attention_kernel);
-      if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
-      if (fa.numRegs != kLaunchRegs)
-        return fail(MLA_ERR_UNSUPPORTED, "attention kernel built with %d registers per thread, expected %d",
-                    fa.numRegs, kLaunchRegs);
-      checked[dev] = 1;
-    }
+  prm.q_base = static_cast<const uint8_t*>(q->data);
+  prm.q_tok = q->stride[0] * es;
+  prm.q_head = q->stride[1] * es;
+  prm.Tq = static_cast<uint32_t>(Tq);
+  if (fp8) {
+    prm.q_scale = q->scale;
+    prm.k_scale = k_nope->scale;
+    prm.v_scale = v->scale;
+    prm.rope_scales = k_rope_pages->scale;
   }
-  const int attn_smem = static_cast<int>(sizeof(Smem) + 1024);
-  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(mla_attention_kernel), attn_smem, dev, 2)) != MLA_OK)
-    return st;
-  schedule_kernel<<<1, kSchedThreads, sched_smem, cs>>>(
-      row_offsets, cache_lens, static_cast<uint32_t>(B), static_cast<uint32_t>(H),
-      static_cast<uint32_t>(Tq), static_cast<uint32_t>(Sk), static_cast<uint32_t>(P),
-      static_cast<uint32_t>(max_pages), 2u * (128 + 128), static_cast<uint8_t*>(workspace));
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "scheduler launch: %s", cudaGetErrorString(e));
-  mla_attention_kernel<<<sms, kThreads, attn_smem, cs>>>(prm);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
-  return MLA_OK;
+  auto launch = fp8 ? launch_attention<true> : launch_attention<false>;
+  return launch(prm, dev, sms, row_offsets, cache_lens, static_cast<uint32_t>(B), static_cast<uint32_t>(H),
+                static_cast<uint32_t>(Tq), static_cast<uint32_t>(Sk), static_cast<uint32_t>(P),
+                static_cast<uint32_t>(max_pages), workspace, cs);
 }
 
 // ------------------------------------------------------------ no-allocation entry point

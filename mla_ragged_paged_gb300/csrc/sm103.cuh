@@ -141,6 +141,14 @@ __device__ __forceinline__ void umma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uin
       " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
+// kind::f8f6f4 with A (e4m3, four per 32-bit column) read from tensor memory.
+__device__ __forceinline__ void umma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
 // Arrive once on `bar` when every previously issued tcgen05.mma of this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -206,6 +214,12 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
       MLA_W8(0), MLA_W8(8)
       : "memory");
 }
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      MLA_W8(0)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
@@ -258,6 +272,27 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+// Four e4m3 codes (byte 0 first) -> four floats (exact).
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t v, float& f0, float& f1, float& f2, float& f3) {
+  uint32_t lo, hi;
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n"
+      " cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(v));
+  asm("{\n .reg .f16 h0, h1;\n mov.b32 {h0, h1}, %2;\n cvt.f32.f16 %0, h0;\n cvt.f32.f16 %1, h1;\n}\n"
+      : "=f"(f0), "=f"(f1)
+      : "r"(lo));
+  asm("{\n .reg .f16 h0, h1;\n mov.b32 {h0, h1}, %2;\n cvt.f32.f16 %0, h0;\n cvt.f32.f16 %1, h1;\n}\n"
+      : "=f"(f2), "=f"(f3)
+      : "r"(hi));
+}
+// Two floats -> two e4m3 codes (round to nearest even, saturating), lo in byte 0.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -96,6 +96,21 @@ def test_ragged_rejects_bad_arguments(lib, change):
     assert lib.mla_last_error_string()
 
 
+def test_fp8_needs_scales(lib):
+    fp8 = binding.MLA_DTYPE_FP8_E4M3
+    a = _ragged_args(q=_desc([10, 2, 192], fp8), k=_desc([20, 2, 128], fp8),
+                     v=_desc([20, 2, 128], fp8), rope=_desc([4, 16, 64], fp8))
+    assert _call_ragged(lib, a) == binding.MLA_ERR_INVALID_ARG
+    assert b"scale" in lib.mla_last_error_string()
+    for t in (a["q"], a["k"], a["v"]):
+        t.scale = 0x50000
+        t.scale_gran = binding.MLA_SCALE_PER_TENSOR
+    assert _call_ragged(lib, a) == binding.MLA_ERR_INVALID_ARG     # rope scales still missing
+    assert b"per-token" in lib.mla_last_error_string()
+    mixed = _ragged_args(q=_desc([10, 2, 192], fp8))                 # fp8 q with bf16 k
+    assert _call_ragged(lib, mixed) == binding.MLA_ERR_INVALID_ARG
+
+
 def test_ragged_rejects_unaligned_stride(lib):
     q = _desc([10, 2, 192])
     q.stride[1] = 196          # 392 bytes: not a multiple of 16

@@ -1,7 +1,8 @@
 """GPU attention (mla_prefill_ragged through the C ABI) versus the float64
 oracle, element by element.
 
-Tolerance (bf16 inputs, bf16 output): |gpu - ref| <= 2e-2 + 2e-2 * |ref|.
+Tolerance (bf16 output): |gpu - ref| <= 2e-2 + 2e-2 * |ref| for bf16 inputs and
+6e-2 + 6e-2 * |ref| for fp8-e4m3 inputs, the oracle taking the dequantised values.
 Small workloads are compared in full; the full-size workloads run in the same
 launch configuration as the benchmark and are compared on sampled rows and
 heads, which the oracle computes one (sequence, head) at a time.
@@ -16,6 +17,7 @@ from oracle import attention as oatt
 pytestmark = pytest.mark.gpu
 
 ATOL = RTOL = 2e-2
+ATOL8 = RTOL8 = 6e-2
 
 
 def run_gpu(w, workspace=None):
@@ -31,6 +33,10 @@ def run_gpu(w, workspace=None):
                            v_scale=d.get("v_scale"), k_rope_scales=d.get("k_rope_scales"))
     status = binding.device_status(ws)
     return out.float().cpu().numpy().astype(np.float64), status
+
+
+def tol(w):
+    return (ATOL8, RTOL8) if w.spec.dtype == "fp8" else (ATOL, RTOL)
 
 
 def assert_close(got, ref, what, atol=ATOL, rtol=RTOL):
@@ -76,7 +82,7 @@ def test_edge_cases(lib, case):
         w.scale = 0.0
     got, status = run_gpu(w)
     assert status == 0
-    assert_close(got, oatt.reference(w), case)
+    assert_close(got, oatt.reference(w), case, *tol(w))
 
 
 def test_many_sequences_random(lib):
@@ -108,7 +114,7 @@ def _sample_rows(w, per_seq=12, seed=0):
     return rows
 
 
-@pytest.mark.parametrize("name", ["deepseek_v3_bf16", "long_context_bf16"])
+@pytest.mark.parametrize("name", ["deepseek_v3_bf16", "long_context_bf16", "fp8_e4m3"])
 def test_full_size_sampled(lib, name):
     w = workloads.generate(workloads.config(name))
     got, status = run_gpu(w)
@@ -116,7 +122,28 @@ def test_full_size_sampled(lib, name):
     assert np.isfinite(got).all(), "every output row must be written and finite"
     heads = [0, w.heads // 3, w.heads - 1]
     ref = oatt.reference(w, heads=heads, rows=_sample_rows(w))
-    assert_close(got, ref, name)
+    assert_close(got, ref, name, *tol(w))
+
+
+FP8_CASES = {
+    "fp8_single_key": dict(n=[1], prior=[0]),
+    "fp8_ragged_tails": dict(n=[300, 0, 129, 256, 257, 1], prior=[0, 5, 1000, 127, 3, 77]),
+    "fp8_page_12": dict(n=[150, 40], prior=[70, 0], page_size=12),
+    "fp8_latent_row_576": dict(n=[140, 60], prior=[10, 130], row_width=576, rope_col=512, page_size=64),
+    "fp8_null_mask": dict(n=[100, 130], prior=[50, 300], mask="null"),
+    "fp8_many_heads": dict(n=[260, 20, 513], prior=[1, 0, 2], heads=16),
+}
+
+
+@pytest.mark.parametrize("case", list(FP8_CASES))
+def test_fp8_cases(lib, case):
+    kw = dict(heads=2, page_size=16, seed=600 + list(FP8_CASES).index(case), dtype="fp8")
+    kw.update(FP8_CASES[case])
+    n, prior = kw.pop("n"), kw.pop("prior")
+    w = workloads.custom(n, prior, **kw)
+    got, status = run_gpu(w)
+    assert status == 0
+    assert_close(got, oatt.reference(w), case, ATOL8, RTOL8)
 
 
 def test_bad_page_id_sets_status(lib):
