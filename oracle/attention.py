@@ -79,25 +79,32 @@ def attention_rows(q_rows, k_full, v, allowed, scale):
     return p @ v
 
 
-def reference(w, heads=None, rows=None, row_block=1024):
+def reference(w, heads=None, rows=None, row_block=1024, out=None):
     """Oracle output [total_q_tokens, H, 128] float64 (NaN where not computed).
 
     heads: iterable of head indices (default all).
-    rows:  optional dict b -> array of local query indices (default all)."""
+    rows:  optional dict b -> array of local query indices; when given, only
+           the sequences it names are computed (default: every row).
+    out:   optional preallocated float64 [total_q_tokens, H, 128] to write the
+           computed rows into (other entries are left untouched)."""
     fp8 = w.spec.dtype == "fp8"
     H = w.heads
     heads = list(range(H)) if heads is None else list(heads)
     q_raw = _raw(w.q, fp8)
     k_raw = _raw(w.k_nope, fp8)
     v_raw = _raw(w.v, fp8)
-    out = np.full((w.total_q, H, DV), np.nan, dtype=np.float64)
+    if out is None:
+        out = np.full((w.total_q, H, DV), np.nan, dtype=np.float64)
     G = 0
     for b in range(w.batch):
         n = int(w.n[b])
         prior = int(w.prior[b])
         L = prior + n
         q0 = int(w.row_offsets[b])
-        sel = np.arange(n) if rows is None or b not in rows else np.asarray(rows[b], dtype=np.int64)
+        if rows is None:
+            sel = np.arange(n)
+        else:
+            sel = np.asarray(rows.get(b, []), dtype=np.int64)
         if n == 0 or sel.size == 0:
             G += L
             continue
