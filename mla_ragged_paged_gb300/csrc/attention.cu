@@ -327,6 +327,37 @@ __device__ __forceinline__ Ring<Cfg<FP8>::kRing> make_ring(Smem<FP8>& s) {
                                smem_u32(&s.ring[0][0])};
 }
 
+// Ring positions of one KV tile.  bf16: K_nope[0:64], K_nope[64:128], K_rope,
+// then the V pair; when V[:, 0:64] would land in the last slot the tile skips
+// that slot (a pad position that carries no data) so the two V chunks are
+// adjacent in shared memory and one N=128 UMMA can span them.  fp8: K_nope,
+// K_rope, V.
+struct TilePos {
+  uint32_t k, v, pad, next;  // pad == kNoPad when the tile has no pad slot
+};
+constexpr uint32_t kNoPad = 0xFFFFFFFFu;
+template <bool FP8>
+__device__ __forceinline__ TilePos tile_pos(uint32_t start) {
+  using C = Cfg<FP8>;
+  TilePos t;
+  t.k = start;
+  if (FP8) {
+    t.v = start + 2;
+    t.pad = kNoPad;
+    t.next = start + 3;
+  } else {
+    uint32_t v = start + 3;
+    t.pad = kNoPad;
+    if (v % C::kRing == C::kRing - 1) {
+      t.pad = v;
+      ++v;
+    }
+    t.v = v;
+    t.next = v + 2;
+  }
+  return t;
+}
+
 // Reads the next work item from the item ring (every consumer warp reads
 // every item; lane 0 releases the slot after the whole warp has read it).
 template <bool FP8>
@@ -462,8 +493,16 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
         alive = load_chunk(&p.tm_k, 0, it, j) && load_chunk(&p.tm_k, 64, it, j) && load_rope(it, j);
       }
       if (alive && j == 0) alive = load_q(0, it) && (it.n1 == 0 || load_q(1, it));
-      if (FP8) alive = alive && load_chunk(&p.tm_v, 0, it, j);
-      else alive = alive && load_chunk(&p.tm_v, 0, it, j) && load_chunk(&p.tm_v, 64, it, j);
+      if (FP8) {
+        alive = alive && load_chunk(&p.tm_v, 0, it, j);
+      } else {
+        if (alive && pos % C::kRing == C::kRing - 1) {  // pad slot: keep the V pair adjacent
+          alive = acquire(pos);
+          if (alive && lane == 0) mbar_arrive(ring.full_bar(pos));
+          ++pos;
+        }
+        alive = alive && load_chunk(&p.tm_v, 0, it, j) && load_chunk(&p.tm_v, 64, it, j);
+      }
     }
   }
   if (status) atomicOr(&hdr->status, status);
@@ -585,7 +624,7 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort
   // Instruction descriptors (fp32 accumulate): bf16 A/B (format 1) or e4m3 (format 0).
   const uint32_t idS = make_idesc(128, 128, 1, false);     // bf16 S (whole S, or fp8's rope part)
   const uint32_t idS8 = make_idesc(128, 128, 0, false);    // fp8 nope part of S
-  const uint32_t idPV = make_idesc(128, 64, 1, true);      // bf16 P.V, N = 64 per V chunk
+  const uint32_t idPV = make_idesc(128, 128, 1, true);     // bf16 P.V, N = 128 over the V pair
   const uint32_t idPV8 = make_idesc(128, 128, 0, true);    // fp8 P.V, N = 128
   const uint32_t q_smem0 = smem_u32(&s.q[0][0][0]);
   uint32_t pos = 0, item_k = 0, qf[2] = {0, 0}, pf[2] = {0, 0}, oe[2] = {0, 0};
@@ -632,14 +671,12 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort
       for (int ks = 0; ks < 4; ++ks)
         umma_f8_ts(d, a0 + ks * 8, v0 + ks * (4096 >> 4), idPV8, ks ? 1u : acc0);
     } else {
-      // one N=64 UMMA per V chunk and K-step of 16 keys.
-      const uint64_t v0 = sw128_desc_at(ring.buf(vpos)), v1 = sw128_desc_at(ring.buf(vpos + 1));
+      // 8 K-steps of 16 keys, N = 128: the two V chunks sit in adjacent slots,
+      // 16 KB apart (the leading byte offset between the two 64-column atoms).
+      const uint64_t v0 = sw128_desc(ring.buf(vpos), kChunk, 1024);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t en = ks ? 1u : acc0;
-        umma_f16_ts(d, a0 + ks * 8, v0 + ks * (2048 >> 4), idPV, en);
-        umma_f16_ts(d + 64, a0 + ks * 8, v1 + ks * (2048 >> 4), idPV, en);
-      }
+      for (int ks = 0; ks < 8; ++ks)
+        umma_f16_ts(d, a0 + ks * 8, v0 + ks * (2048 >> 4), idPV, ks ? 1u : acc0);
     }
   };
   auto release = [&](uint32_t first, int count) {
@@ -667,8 +704,8 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort
     if (!it.valid) break;
     const bool has1 = it.n1 > 0;
     const int nkv = has1 ? it.nkv1 : it.nkv0;
-    auto kpos = [&](int j) { return pos + C::kCPT * j; };
-    alive = wait_chunks(kpos(0), kK);
+    TilePos cur = tile_pos<FP8>(pos);
+    alive = wait_chunks(cur.k, kK);
     alive = alive && mbar_wait(smem_u32(&s.q_full[0]), qf[0] & 1u, abort);
     ++qf[0];
     if (alive && has1) {
@@ -677,26 +714,31 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort
     }
     if (!alive) break;
     tc_fence_after();
-    issue_s(0, kpos(0));
-    if (has1) issue_s(1, kpos(0));
-    release(kpos(0), kK);
+    issue_s(0, cur.k);
+    if (has1) issue_s(1, cur.k);
+    release(cur.k, kK);
     for (int j = 0; j < nkv && alive; ++j) {
       const bool on0 = j < it.nkv0;
       const bool next0 = j + 1 < it.nkv0;
       const bool next1 = has1 && j + 1 < nkv;
+      const TilePos nxt = tile_pos<FP8>(cur.next);
       bool k_next = false;  // K chunks of tile j+1 waited for
       auto need_k_next = [&]() -> bool {
         if (k_next) return true;
         k_next = true;
-        return wait_chunks(kpos(j + 1), kK);
+        return wait_chunks(nxt.k, kK);
       };
-      if (!(alive = wait_chunks(kpos(j) + kK, kV))) break;
+      if (cur.pad != kNoPad) {  // pass the empty pad slot straight back
+        if (!(alive = wait_chunks(cur.pad, 1))) break;
+        release(cur.pad, 1);
+      }
+      if (!(alive = wait_chunks(cur.v, kV))) break;
       if (on0) {
         if (!(alive = wait_p(0, j == 0))) break;
-        issue_pv(0, kpos(j) + kK, j > 0);
+        issue_pv(0, cur.v, j > 0);
         if (next0) {
           if (!(alive = need_k_next())) break;
-          issue_s(0, kpos(j + 1));
+          issue_s(0, nxt.k);
         } else {
           umma_commit(smem_u32(&s.o_full[0]));
           umma_commit(smem_u32(&s.q_empty[0]));
@@ -704,21 +746,22 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort
       }
       if (has1) {
         if (!(alive = wait_p(1, j == 0))) break;
-        issue_pv(1, kpos(j) + kK, j > 0);
-        release(kpos(j) + kK, kV);
+        issue_pv(1, cur.v, j > 0);
+        release(cur.v, kV);
         if (next1) {
           if (!(alive = need_k_next())) break;
-          issue_s(1, kpos(j + 1));
+          issue_s(1, nxt.k);
         } else {
           umma_commit(smem_u32(&s.o_full[1]));
           umma_commit(smem_u32(&s.q_empty[1]));
         }
       } else {
-        release(kpos(j) + kK, kV);
+        release(cur.v, kV);
       }
-      if (next0 || next1) release(kpos(j + 1), kK);
+      if (next0 || next1) release(nxt.k, kK);
+      cur = nxt;
     }
-    pos += C::kCPT * nkv;
+    pos = cur.k;
   }
   // Make sure no UMMA is still in flight before tensor memory is released.
   umma_commit(smem_u32(&s.drain));
