@@ -372,6 +372,12 @@ __device__ __forceinline__ bool read_item(Smem<FP8>& s, uint32_t& item_k, int la
   return true;
 }
 
+// Full barriers are per group, not per chunk: every TMA box of a tile's K
+// chunks (and of its V pair) signals the full barrier of the group's first
+// slot with one expect_tx for the summed bytes, so the UMMA thread waits once
+// per group.  A slot's full barrier therefore completes a phase only when the
+// slot heads a group; both sides keep one phase bit per slot.  Empty barriers
+// stay per chunk (one UMMA commit each).
 template <bool FP8>
 __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volatile uint32_t* abort) {
   using C = Cfg<FP8>;
@@ -380,81 +386,120 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
   const auto ring = make_ring(s);
   uint32_t pos = 0, item_k = 0, q_uses[2] = {0, 0};
   uint32_t status = 0;
+  uint32_t fph = 0;                  // full-barrier phase bit per slot (flipped per head use)
+  uint32_t recent[C::kRing] = {};    // last group heads issued, for the abort drain
+  uint32_t nrecent = 0;
   bool alive = true;
+  // fp8 full barriers count three arrivals (the converter warps add two to a K group).
+  constexpr int kExtraArrivals = FP8 ? 2 : 0;
 
   auto acquire = [&](uint32_t ps) -> bool {
     return mbar_wait(ring.empty_bar(ps), ring.phase(ps) ^ 1u, abort);
   };
-  // One 16 KB TMA box (128 rows) of k_nope or v into the next ring slot.
-  auto load_chunk = [&](const CUtensorMap* map, int x, const ItemInfo& it, int j) -> bool {
-    if (!acquire(pos)) return false;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(ring.full_bar(pos), kChunk);
-      if (FP8) mbar_arrive(ring.full_bar(pos));  // fp8 slots count two arrivals
-      tma_load_3d(ring.buf(pos), map, ring.full_bar(pos), x, it.h, it.kv_row0 + j * kBN);
+  auto note_head = [&](uint32_t head) {
+    recent[nrecent % C::kRing] = (ring.slot(head) << 1) | ((fph >> ring.slot(head)) & 1u);
+    ++nrecent;
+    fph ^= 1u << ring.slot(head);
+  };
+  // TMA of 128 rows (one 16 KB chunk) of k_nope or v into slot `ps`, signalling `bar`.
+  auto tma_chunk = [&](const CUtensorMap* map, int x, const ItemInfo& it, int j, uint32_t ps, uint32_t bar) {
+    tma_load_3d(ring.buf(ps), map, bar, x, it.h, it.kv_row0 + j * kBN);
+  };
+  // bf16 K_rope rows into slot `ps`: TMA boxes (one per page segment, lane t
+  // owns box t) when pages are 8-row aligned, else a swizzled row gather.
+  // Returns the bytes the TMA boxes will deliver (0 for the gather).
+  auto rope_lookup = [&](const ItemInfo& it, int j, uint32_t& page, uint32_t& row_in_page) -> bool {
+    const int nbox = kBN / static_cast<int>(p.rope_box);
+    bool issue = false;
+    if (lane < nbox) {
+      const int key = j * kBN + lane * static_cast<int>(p.rope_box);
+      if (key < it.L) {
+        const uint32_t col = static_cast<uint32_t>(key) / p.page_size;
+        row_in_page = static_cast<uint32_t>(key) - col * p.page_size;
+        if (col >= p.max_pages) {
+          status |= MLA_DEVICE_STATUS_BAD_COLUMN;
+        } else {
+          page = p.page_table[static_cast<long long>(it.b) * p.pt_stride + col];
+          if (page >= p.num_pages) status |= MLA_DEVICE_STATUS_BAD_PAGE;
+          else issue = true;
+        }
+      }
     }
-    ++pos;
+    return issue;
+  };
+  auto rope_gather = [&](const ItemInfo& it, int j, uint32_t ps) {
+    const uint32_t dst = ring.buf(ps);
+    for (int r = lane; r < kBN; r += 32) {
+      const int key = j * kBN + r;
+      if (key >= it.L) continue;
+      const uint32_t col = static_cast<uint32_t>(key) / p.page_size;
+      if (col >= p.max_pages) { status |= MLA_DEVICE_STATUS_BAD_COLUMN; continue; }
+      const uint32_t page = p.page_table[static_cast<long long>(it.b) * p.pt_stride + col];
+      if (page >= p.num_pages) { status |= MLA_DEVICE_STATUS_BAD_PAGE; continue; }
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.rope_base + page * p.rope_page_bytes +
+          static_cast<long long>(key - static_cast<int>(col * p.page_size)) * p.rope_tok_bytes);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = src[c];
+        const uint32_t a = dst + r * 128 + ((c ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+  };
+  // The K group of tile j: bf16 K_nope[0:64], K_nope[64:128], K_rope at
+  // positions k..k+2; fp8 K_nope at k (the converters fill K_rope at k+1).
+  auto load_k_group = [&](const ItemInfo& it, int j, uint32_t k) -> bool {
+    const uint32_t bar = ring.full_bar(k);
+    if (FP8) {
+      if (!acquire(k)) return false;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, kChunk);
+        tma_chunk(&p.tm_k, 0, it, j, k, bar);
+      }
+    } else {
+      if (!acquire(k) || !acquire(k + 1) || !acquire(k + 2)) return false;
+      if (!p.rope_manual) {
+        uint32_t page = 0, row_in_page = 0;
+        const bool issue = rope_lookup(it, j, page, row_in_page);
+        const uint32_t mask = __ballot_sync(0xffffffffu, issue);
+        const uint32_t bytes = 2 * kChunk + __popc(mask) * p.rope_box * 128u;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, bytes);
+          tma_chunk(&p.tm_k, 0, it, j, k, bar);
+          tma_chunk(&p.tm_k, 64, it, j, k + 1, bar);
+        }
+        __syncwarp();
+        if (issue)
+          tma_load_3d(ring.buf(k + 2) + lane * p.rope_box * 128u, &p.tm_rope, bar, 0,
+                      static_cast<int>(row_in_page), static_cast<int>(page));
+      } else {
+        rope_gather(it, j, k + 2);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, 2 * kChunk);
+          tma_chunk(&p.tm_k, 0, it, j, k, bar);
+          tma_chunk(&p.tm_k, 64, it, j, k + 1, bar);
+        }
+      }
+    }
+    note_head(k);
     return true;
   };
-  auto load_rope = [&](const ItemInfo& it, int j) -> bool {
-    if (!acquire(pos)) return false;
-    const int key0 = j * kBN;
-    if (!p.rope_manual) {
-      // One TMA box of rope_box rows per page segment; lane t owns box t.
-      const int nbox = kBN / static_cast<int>(p.rope_box);
-      bool issue = false;
-      uint32_t page = 0, row_in_page = 0;
-      if (lane < nbox) {
-        const int key = key0 + lane * static_cast<int>(p.rope_box);
-        if (key < it.L) {
-          const uint32_t col = static_cast<uint32_t>(key) / p.page_size;
-          row_in_page = static_cast<uint32_t>(key) - col * p.page_size;
-          if (col >= p.max_pages) {
-            status |= MLA_DEVICE_STATUS_BAD_COLUMN;
-          } else {
-            page = p.page_table[static_cast<long long>(it.b) * p.pt_stride + col];
-            if (page >= p.num_pages) status |= MLA_DEVICE_STATUS_BAD_PAGE;
-            else issue = true;
-          }
-        }
-      }
-      const uint32_t mask = __ballot_sync(0xffffffffu, issue);
-      const uint32_t bytes = __popc(mask) * p.rope_box * 128u;
-      if (lane == 0) {
-        if (bytes) mbar_arrive_expect_tx(ring.full_bar(pos), bytes);
-        else mbar_arrive(ring.full_bar(pos));
-      }
-      __syncwarp();
-      if (issue)
-        tma_load_3d(ring.buf(pos) + lane * p.rope_box * 128u, &p.tm_rope, ring.full_bar(pos), 0,
-                    static_cast<int>(row_in_page), static_cast<int>(page));
-    } else {
-      // Row-by-row gather into the 128B-swizzled layout.
-      const uint32_t dst = ring.buf(pos);
-      for (int r = lane; r < kBN; r += 32) {
-        const int key = key0 + r;
-        if (key >= it.L) continue;
-        const uint32_t col = static_cast<uint32_t>(key) / p.page_size;
-        if (col >= p.max_pages) { status |= MLA_DEVICE_STATUS_BAD_COLUMN; continue; }
-        const uint32_t page = p.page_table[static_cast<long long>(it.b) * p.pt_stride + col];
-        if (page >= p.num_pages) { status |= MLA_DEVICE_STATUS_BAD_PAGE; continue; }
-        const uint4* src = reinterpret_cast<const uint4*>(
-            p.rope_base + page * p.rope_page_bytes +
-            static_cast<long long>(key - static_cast<int>(col * p.page_size)) * p.rope_tok_bytes);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = src[c];
-          const uint32_t a = dst + r * 128 + ((c ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
-                       "r"(v.z), "r"(v.w)
-                       : "memory");
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ring.full_bar(pos));
+  // The V group of tile j: bf16 V[:, 0:64], V[:, 64:128] at v, v+1; fp8 V at v.
+  auto load_v_group = [&](const ItemInfo& it, int j, uint32_t v) -> bool {
+    const uint32_t bar = ring.full_bar(v);
+    if (!acquire(v) || (!FP8 && !acquire(v + 1))) return false;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, (FP8 ? 1 : 2) * kChunk);
+      for (int e = 0; e < kExtraArrivals; ++e) mbar_arrive(bar);
+      tma_chunk(&p.tm_v, 0, it, j, v, bar);
+      if (!FP8) tma_chunk(&p.tm_v, 64, it, j, v + 1, bar);
     }
-    ++pos;
+    note_head(v);
     return true;
   };
   // bf16: the whole 192-wide Q tile (three 64-dim atoms).  fp8: the 128
@@ -486,30 +531,28 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     if (!it.valid) break;
     const int nkv = it.n1 > 0 ? it.nkv1 : it.nkv0;
     for (int j = 0; j < nkv && alive; ++j) {
-      if (FP8) {
-        alive = load_chunk(&p.tm_k, 0, it, j);
-        ++pos;  // the converter warps fill the K_rope slot
-      } else {
-        alive = load_chunk(&p.tm_k, 0, it, j) && load_chunk(&p.tm_k, 64, it, j) && load_rope(it, j);
-      }
+      const TilePos tp = tile_pos<FP8>(pos);
+      alive = load_k_group(it, j, tp.k);
       if (alive && j == 0) alive = load_q(0, it) && (it.n1 == 0 || load_q(1, it));
-      if (FP8) {
-        alive = alive && load_chunk(&p.tm_v, 0, it, j);
-      } else {
-        if (alive && pos % C::kRing == C::kRing - 1) {  // pad slot: keep the V pair adjacent
-          alive = acquire(pos);
-          if (alive && lane == 0) mbar_arrive(ring.full_bar(pos));
-          ++pos;
+      if (alive && tp.pad != kNoPad) {  // pad slot: keeps the V pair adjacent
+        alive = acquire(tp.pad);
+        if (alive) {
+          if (lane == 0) mbar_arrive(ring.full_bar(tp.pad));
+          note_head(tp.pad);
         }
-        alive = alive && load_chunk(&p.tm_v, 0, it, j) && load_chunk(&p.tm_v, 64, it, j);
       }
+      alive = alive && load_v_group(it, j, tp.v);
+      pos = tp.next;
     }
   }
   if (status) atomicOr(&hdr->status, status);
   if (*abort) {
     // Let every copy this warp started land before the CTA exits.
-    for (uint32_t ps = pos > C::kRing ? pos - C::kRing : 0; ps < pos; ++ps)
-      if (!FP8 || ps % C::kCPT != 1) wait_drain(ring.full_bar(ps), ring.phase(ps));
+    const uint32_t n = nrecent < C::kRing ? nrecent : C::kRing;
+    for (uint32_t i = 0; i < n; ++i) {
+      const uint32_t e = recent[(nrecent - 1 - i) % C::kRing];
+      wait_drain(ring.full + 8u * (e >> 1), e & 1u);
+    }
     for (int q = 0; q < 2; ++q)
       if (q_uses[q]) wait_drain(smem_u32(&s.q_full[q]), (q_uses[q] - 1) & 1u);
   }
@@ -581,9 +624,10 @@ __device__ void converter_warps(Smem<true>& s, const AttnParams& p, int cl, vola
     signal(smem_u32(&s.q_full[q]));
     return true;
   };
-  auto conv_rope = [&](const ItemInfo& it, int j) -> bool {
-    if (!mbar_wait(ring.empty_bar(pos), ring.phase(pos) ^ 1u, abort)) return false;
-    const uint32_t dst = ring.buf(pos);
+  // Tile j's K_rope goes to slot k+1 and completes the K group headed by slot k.
+  auto conv_rope = [&](const ItemInfo& it, int j, uint32_t k) -> bool {
+    if (!mbar_wait(ring.empty_bar(k + 1), ring.phase(k + 1) ^ 1u, abort)) return false;
+    const uint32_t dst = ring.buf(k + 1);
     for (int r = cl; r < kBN; r += 64) {
       const int key = j * kBN + r;
       if (key >= it.L) continue;  // masked keys: stale data is never used
@@ -597,8 +641,7 @@ __device__ void converter_warps(Smem<true>& s, const AttnParams& p, int cl, vola
       load_e4m3_row(p.rope_base + page * p.rope_page_bytes + in_page * p.rope_tok_bytes, sc, f);
       store_bf16_row(dst, r, f);
     }
-    signal(ring.full_bar(pos));
-    ++pos;
+    signal(ring.full_bar(k));
     return true;
   };
 
@@ -607,10 +650,10 @@ __device__ void converter_warps(Smem<true>& s, const AttnParams& p, int cl, vola
     if (!read_item(s, item_k, lane, it, abort) || !it.valid) break;
     const int nkv = it.n1 > 0 ? it.nkv1 : it.nkv0;
     for (int j = 0; j < nkv && alive; ++j) {
-      pos += 1;  // K_nope slot (producer)
-      alive = conv_rope(it, j);
+      const TilePos tp = tile_pos<true>(pos);
+      alive = conv_rope(it, j, tp.k);
       if (alive && j == 0) alive = conv_q(0, it) && (it.n1 == 0 || conv_q(1, it));
-      pos += 1;  // V slot (producer)
+      pos = tp.next;
     }
     (void)C::kCPT;
   }
@@ -630,9 +673,11 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort
   uint32_t pos = 0, item_k = 0, qf[2] = {0, 0}, pf[2] = {0, 0}, oe[2] = {0, 0};
   bool alive = true;
 
-  auto wait_chunks = [&](uint32_t first, int count) -> bool {
-    for (int c = 0; c < count; ++c)
-      if (!mbar_wait(ring.full_bar(first + c), ring.phase(first + c), abort)) return false;
+  uint32_t fph = 0;  // full-barrier phase bit per slot, flipped at each use as a group head
+  auto wait_group = [&](uint32_t head) -> bool {
+    const uint32_t sl = ring.slot(head);
+    if (!mbar_wait(ring.full_bar(head), (fph >> sl) & 1u, abort)) return false;
+    fph ^= 1u << sl;
     tc_fence_after();
     return true;
   };
@@ -705,7 +750,7 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort
     const bool has1 = it.n1 > 0;
     const int nkv = has1 ? it.nkv1 : it.nkv0;
     TilePos cur = tile_pos<FP8>(pos);
-    alive = wait_chunks(cur.k, kK);
+    alive = wait_group(cur.k);
     alive = alive && mbar_wait(smem_u32(&s.q_full[0]), qf[0] & 1u, abort);
     ++qf[0];
     if (alive && has1) {
@@ -726,13 +771,13 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort
       auto need_k_next = [&]() -> bool {
         if (k_next) return true;
         k_next = true;
-        return wait_chunks(nxt.k, kK);
+        return wait_group(nxt.k);
       };
       if (cur.pad != kNoPad) {  // pass the empty pad slot straight back
-        if (!(alive = wait_chunks(cur.pad, 1))) break;
+        if (!(alive = wait_group(cur.pad))) break;
         release(cur.pad, 1);
       }
-      if (!(alive = wait_chunks(cur.v, kV))) break;
+      if (!(alive = wait_group(cur.v))) break;
       if (on0) {
         if (!(alive = wait_p(0, j == 0))) break;
         issue_pv(0, cur.v, j > 0);
@@ -947,9 +992,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
       mbar_init(smem_u32(&s.o_empty[i]), 4);
     }
     for (int i = 0; i < C::kRing; ++i) {
-      // fp8: a K_rope slot is filled by two converter warps, so every slot
-      // takes two arrivals (the producer arrives twice on its own slots).
-      mbar_init(smem_u32(&s.kv_full[i]), FP8 ? 2 : 1);
+      // Full barriers are per group (see producer_warp).  fp8: a K group is
+      // completed by the producer's TMA and the two converter warps, so every
+      // full barrier takes three arrivals (the producer adds two to V groups).
+      mbar_init(smem_u32(&s.kv_full[i]), FP8 ? 3 : 1);
       mbar_init(smem_u32(&s.kv_empty[i]), 1);
     }
     mbar_init(smem_u32(&s.drain), 1);
