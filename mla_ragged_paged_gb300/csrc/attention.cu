@@ -14,8 +14,9 @@
 // Warp roles (384 threads = three warpgroups, one warp of each per SM
 // sub-partition):
 //   warp 0      producer: work-item fetch (atomic counter), TMA loads
-//   warp 1      UMMA issuer (one thread) and tensor-memory owner
-//   warps 2-3   fp8 inputs only: K_rope / Q_rope conversion (else idle)
+//   warp 1      UMMA issuer for Q0 (one thread) and tensor-memory owner
+//   warp 2      UMMA issuer for Q1 (one thread)
+//   warp 3      fp8 inputs only: K_rope / Q_rope conversion (else idle)
 //   warps 4-7   softmax + epilogue for Q0
 //   warps 8-11  softmax + epilogue for Q1
 // A warp may only touch TMEM lanes 32*(warp%4) .. +31, so each softmax
@@ -126,7 +127,7 @@ struct __align__(1024) Smem {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[Cfg<FP8>::kRing], kv_empty[Cfg<FP8>::kRing];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
-  uint64_t drain;
+  uint64_t drain[2];
   ItemInfo items[2];
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -390,8 +391,8 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
   uint32_t recent[C::kRing] = {};    // last group heads issued, for the abort drain
   uint32_t nrecent = 0;
   bool alive = true;
-  // fp8 full barriers count three arrivals (the converter warps add two to a K group).
-  constexpr int kExtraArrivals = FP8 ? 2 : 0;
+  // fp8 full barriers count two arrivals (the converter warp adds one to a K group).
+  constexpr int kExtraArrivals = FP8 ? 1 : 0;
 
   auto acquire = [&](uint32_t ps) -> bool {
     return mbar_wait(ring.empty_bar(ps), ring.phase(ps) ^ 1u, abort);
@@ -503,7 +504,7 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     return true;
   };
   // bf16: the whole 192-wide Q tile (three 64-dim atoms).  fp8: the 128
-  // nope codes only; the converter warps write the rope part.
+  // nope codes only; the converter warp writes the rope part.
   auto load_q = [&](int q, const ItemInfo& it) -> bool {
     const uint32_t bar = smem_u32(&s.q_full[q]);
     if (!mbar_wait(smem_u32(&s.q_empty[q]), (q_uses[q] & 1u) ^ 1u, abort)) return false;
@@ -558,13 +559,13 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
   }
 }
 
-// fp8 inputs: warps 2 and 3 turn the rope parts into bf16 UMMA operands.
+// fp8 inputs: warp 3 turns the rope parts into bf16 UMMA operands.
 //   Q_rope:  64 e4m3 codes per query row -> bf16 (exact), 128B-swizzled.
 //   K_rope:  per key, the paged pool row (64 codes) times s_r[slot] / s_k,
 //            rounded to bf16, so that q_rope . k_rope' shares the s_q s_k
 //            factor of the nope part.
-// Each lane owns two of the 128 rows; each warp signals the slot's mbarrier
-// once its rows are written (kv_full / q_full count both warps).
+// Each lane owns four of the 128 rows; the warp signals the group's mbarrier
+// once its rows are written.
 __device__ __forceinline__ void store_bf16_row(uint32_t dst, int r, const float (&f)[64]) {
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
@@ -592,11 +593,10 @@ __device__ __forceinline__ void load_e4m3_row(const uint8_t* src, float scale, f
     }
   }
 }
-__device__ void converter_warps(Smem<true>& s, const AttnParams& p, int cl, volatile uint32_t* abort) {
+__device__ void converter_warp(Smem<true>& s, const AttnParams& p, int lane, volatile uint32_t* abort) {
   using C = Cfg<true>;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
   const auto ring = make_ring(s);
-  const int lane = cl & 31;
   const float inv_sk = 1.f / *p.k_scale;
   uint32_t pos = 0, item_k = 0, q_uses[2] = {0, 0}, status = 0;
   bool alive = true;
@@ -610,7 +610,7 @@ __device__ void converter_warps(Smem<true>& s, const AttnParams& p, int cl, vola
     if (!mbar_wait(smem_u32(&s.q_empty[q]), (q_uses[q] & 1u) ^ 1u, abort)) return false;
     ++q_uses[q];
     const uint32_t dst = smem_u32(&s.q[q][1][0]);
-    for (int r = cl; r < kBM; r += 64) {
+    for (int r = lane; r < kBM; r += 32) {
       const int row = it.q_row0 + q * kBM + r;
       float f[64];
       if (row < static_cast<int>(p.Tq)) {
@@ -628,7 +628,7 @@ __device__ void converter_warps(Smem<true>& s, const AttnParams& p, int cl, vola
   auto conv_rope = [&](const ItemInfo& it, int j, uint32_t k) -> bool {
     if (!mbar_wait(ring.empty_bar(k + 1), ring.phase(k + 1) ^ 1u, abort)) return false;
     const uint32_t dst = ring.buf(k + 1);
-    for (int r = cl; r < kBN; r += 64) {
+    for (int r = lane; r < kBN; r += 32) {
       const int key = j * kBN + r;
       if (key >= it.L) continue;  // masked keys: stale data is never used
       const uint32_t col = static_cast<uint32_t>(key) / p.page_size;
@@ -660,8 +660,14 @@ __device__ void converter_warps(Smem<true>& s, const AttnParams& p, int cl, vola
   if (status) atomicOr(&hdr->status, status);
 }
 
+// UMMA issue for one query tile.  Warps 1 and 2 each run this for their own
+// tile (q = 0, 1): a thread blocked on a barrier wait then no longer holds up
+// the other tile's UMMAs.  Both threads walk the same ring and release every
+// chunk (empty barriers count two); a thread with no work on a KV tile still
+// waits for the tile's groups before releasing them, so no barrier phase can
+// be released ahead of its fill.
 template <bool FP8>
-__device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort) {
+__device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t* abort) {
   using C = Cfg<FP8>;
   const auto ring = make_ring(s);
   // Instruction descriptors (fp32 accumulate): bf16 A/B (format 1) or e4m3 (format 0).
@@ -669,8 +675,9 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort
   const uint32_t idS8 = make_idesc(128, 128, 0, false);    // fp8 nope part of S
   const uint32_t idPV = make_idesc(128, 128, 1, true);     // bf16 P.V, N = 128 over the V pair
   const uint32_t idPV8 = make_idesc(128, 128, 0, true);    // fp8 P.V, N = 128
-  const uint32_t q_smem0 = smem_u32(&s.q[0][0][0]);
-  uint32_t pos = 0, item_k = 0, qf[2] = {0, 0}, pf[2] = {0, 0}, oe[2] = {0, 0};
+  const uint64_t qd = sw128_desc_at(smem_u32(&s.q[q][0][0]));
+  const uint32_t d_s = tmem + col_s(q), d_o = tmem + col_o(q);
+  uint32_t pos = 0, item_k = 0, qf = 0, pf = 0, oe = 0;
   bool alive = true;
 
   uint32_t fph = 0;  // full-barrier phase bit per slot, flipped at each use as a group head
@@ -682,17 +689,14 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort
     return true;
   };
   // S_q = Q_q . [K_nope | K_rope]^T.
-  auto issue_s = [&](int q, uint32_t kpos) {
-    const uint64_t qd = sw128_desc_at(q_smem0 + static_cast<uint32_t>(q) * (C::kQChunks * kChunk));
-    const uint32_t d = tmem + col_s(q);
+  auto issue_s = [&](uint32_t kpos) {
     if (FP8) {
       // 4 e4m3 K-steps of 32 over the nope atom, then 4 bf16 K-steps of 16 over rope.
       const uint64_t kd = sw128_desc_at(ring.buf(kpos)), rd = sw128_desc_at(ring.buf(kpos + 1));
 #pragma unroll
-      for (int k = 0; k < 4; ++k) umma_f8_ss(d, qd + 2 * k, kd + 2 * k, idS8, k != 0);
+      for (int k = 0; k < 4; ++k) umma_f8_ss(d_s, qd + 2 * k, kd + 2 * k, idS8, k != 0);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        umma_f16_ss(d, qd + (kChunk >> 4) + 2 * k, rd + 2 * k, idS, 1);
+      for (int k = 0; k < 4; ++k) umma_f16_ss(d_s, qd + (kChunk >> 4) + 2 * k, rd + 2 * k, idS, 1);
     } else {
       // 3 swizzle atoms x 4 K-steps of 16.
 #pragma unroll
@@ -700,39 +704,38 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort
         const uint64_t kd = sw128_desc_at(ring.buf(kpos + a));
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_f16_ss(d, qd + a * (kChunk >> 4) + 2 * k, kd + 2 * k, idS, (a | k) != 0);
+          umma_f16_ss(d_s, qd + a * (kChunk >> 4) + 2 * k, kd + 2 * k, idS, (a | k) != 0);
       }
     }
     umma_commit(smem_u32(&s.s_full[q]));
   };
   // O_q (+)= P_q . V, P from TMEM.
-  auto issue_pv = [&](int q, uint32_t vpos, bool acc) {
-    const uint32_t a0 = tmem + col_s(q), d = tmem + col_o(q);
+  auto issue_pv = [&](uint32_t vpos, bool acc) {
     const uint32_t acc0 = acc ? 1u : 0u;
     if (FP8) {
       // 4 K-steps of 32 keys; P holds four e4m3 per column, V is one MN-major atom.
       const uint64_t v0 = sw128_desc_at(ring.buf(vpos));
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_f8_ts(d, a0 + ks * 8, v0 + ks * (4096 >> 4), idPV8, ks ? 1u : acc0);
+        umma_f8_ts(d_o, d_s + ks * 8, v0 + ks * (4096 >> 4), idPV8, ks ? 1u : acc0);
     } else {
       // 8 K-steps of 16 keys, N = 128: the two V chunks sit in adjacent slots,
       // 16 KB apart (the leading byte offset between the two 64-column atoms).
       const uint64_t v0 = sw128_desc(ring.buf(vpos), kChunk, 1024);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_f16_ts(d, a0 + ks * 8, v0 + ks * (2048 >> 4), idPV, ks ? 1u : acc0);
+        umma_f16_ts(d_o, d_s + ks * 8, v0 + ks * (2048 >> 4), idPV, ks ? 1u : acc0);
     }
   };
   auto release = [&](uint32_t first, int count) {
     for (int c = 0; c < count; ++c) umma_commit(ring.empty_bar(first + c));
   };
-  auto wait_p = [&](int q, bool first_tile) -> bool {
-    if (!mbar_wait(smem_u32(&s.p_full[q]), pf[q] & 1u, abort)) return false;
-    ++pf[q];
+  auto wait_p = [&](bool first_tile) -> bool {
+    if (!mbar_wait(smem_u32(&s.p_full[q]), pf & 1u, abort)) return false;
+    ++pf;
     if (first_tile) {
-      if (!mbar_wait(smem_u32(&s.o_empty[q]), (oe[q] & 1u) ^ 1u, abort)) return false;
-      ++oe[q];
+      if (!mbar_wait(smem_u32(&s.o_empty[q]), (oe & 1u) ^ 1u, abort)) return false;
+      ++oe;
     }
     tc_fence_after();
     return true;
@@ -747,70 +750,50 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, volatile uint32_t* abort
     mbar_arrive(smem_u32(&s.item_empty[islot]));
     ++item_k;
     if (!it.valid) break;
-    const bool has1 = it.n1 > 0;
-    const int nkv = has1 ? it.nkv1 : it.nkv0;
+    const int nkv = it.n1 > 0 ? it.nkv1 : it.nkv0;   // KV tiles the item streams
+    const int mine = q ? (it.n1 > 0 ? it.nkv1 : 0) : it.nkv0;  // tiles this query tile uses
     TilePos cur = tile_pos<FP8>(pos);
     alive = wait_group(cur.k);
-    alive = alive && mbar_wait(smem_u32(&s.q_full[0]), qf[0] & 1u, abort);
-    ++qf[0];
-    if (alive && has1) {
-      alive = mbar_wait(smem_u32(&s.q_full[1]), qf[1] & 1u, abort);
-      ++qf[1];
+    if (alive && mine > 0) {
+      alive = mbar_wait(smem_u32(&s.q_full[q]), qf & 1u, abort);
+      ++qf;
+      if (alive) {
+        tc_fence_after();
+        issue_s(cur.k);
+      }
     }
     if (!alive) break;
-    tc_fence_after();
-    issue_s(0, cur.k);
-    if (has1) issue_s(1, cur.k);
     release(cur.k, kK);
     for (int j = 0; j < nkv && alive; ++j) {
-      const bool on0 = j < it.nkv0;
-      const bool next0 = j + 1 < it.nkv0;
-      const bool next1 = has1 && j + 1 < nkv;
+      const bool on = j < mine;
+      const bool has_next = j + 1 < nkv;
       const TilePos nxt = tile_pos<FP8>(cur.next);
-      bool k_next = false;  // K chunks of tile j+1 waited for
-      auto need_k_next = [&]() -> bool {
-        if (k_next) return true;
-        k_next = true;
-        return wait_group(nxt.k);
-      };
       if (cur.pad != kNoPad) {  // pass the empty pad slot straight back
         if (!(alive = wait_group(cur.pad))) break;
         release(cur.pad, 1);
       }
       if (!(alive = wait_group(cur.v))) break;
-      if (on0) {
-        if (!(alive = wait_p(0, j == 0))) break;
-        issue_pv(0, cur.v, j > 0);
-        if (next0) {
-          if (!(alive = need_k_next())) break;
-          issue_s(0, nxt.k);
-        } else {
-          umma_commit(smem_u32(&s.o_full[0]));
-          umma_commit(smem_u32(&s.q_empty[0]));
-        }
+      if (on) {
+        if (!(alive = wait_p(j == 0))) break;
+        issue_pv(cur.v, j > 0);
       }
-      if (has1) {
-        if (!(alive = wait_p(1, j == 0))) break;
-        issue_pv(1, cur.v, j > 0);
-        release(cur.v, kV);
-        if (next1) {
-          if (!(alive = need_k_next())) break;
-          issue_s(1, nxt.k);
-        } else {
-          umma_commit(smem_u32(&s.o_full[1]));
-          umma_commit(smem_u32(&s.q_empty[1]));
-        }
-      } else {
-        release(cur.v, kV);
+      release(cur.v, kV);
+      if (has_next) {
+        if (!(alive = wait_group(nxt.k))) break;
+        if (j + 1 < mine) issue_s(nxt.k);
+        release(nxt.k, kK);
       }
-      if (next0 || next1) release(nxt.k, kK);
+      if (on && j + 1 == mine) {
+        umma_commit(smem_u32(&s.o_full[q]));
+        umma_commit(smem_u32(&s.q_empty[q]));
+      }
       cur = nxt;
     }
     pos = cur.k;
   }
   // Make sure no UMMA is still in flight before tensor memory is released.
-  umma_commit(smem_u32(&s.drain));
-  wait_drain(smem_u32(&s.drain), 0);
+  umma_commit(smem_u32(&s.drain[q]));
+  wait_drain(smem_u32(&s.drain[q]), 0);
 }
 
 template <bool FP8>
@@ -982,9 +965,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
     s.abort_flag = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.item_full[i]), 1);
-      // MMA thread + 8 softmax warps (+ 2 converter warps for fp8)
-      mbar_init(smem_u32(&s.item_empty[i]), FP8 ? 11 : 9);
-      mbar_init(smem_u32(&s.q_full[i]), FP8 ? 3 : 1);  // TMA (+ two rope converter warps)
+      // 2 UMMA threads + 8 softmax warps (+ the converter warp for fp8)
+      mbar_init(smem_u32(&s.item_empty[i]), FP8 ? 11 : 10);
+      mbar_init(smem_u32(&s.q_full[i]), FP8 ? 2 : 1);  // TMA (+ the rope converter warp)
       mbar_init(smem_u32(&s.q_empty[i]), 1);
       mbar_init(smem_u32(&s.s_full[i]), 1);
       mbar_init(smem_u32(&s.p_full[i]), 4);
@@ -993,12 +976,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
     }
     for (int i = 0; i < C::kRing; ++i) {
       // Full barriers are per group (see producer_warp).  fp8: a K group is
-      // completed by the producer's TMA and the two converter warps, so every
-      // full barrier takes three arrivals (the producer adds two to V groups).
-      mbar_init(smem_u32(&s.kv_full[i]), FP8 ? 3 : 1);
-      mbar_init(smem_u32(&s.kv_empty[i]), 1);
+      // completed by the producer's TMA and the converter warp, so every full
+      // barrier takes two arrivals (the producer adds one to V groups).
+      mbar_init(smem_u32(&s.kv_full[i]), FP8 ? 2 : 1);
+      // Both UMMA threads release every chunk.
+      mbar_init(smem_u32(&s.kv_empty[i]), 2);
     }
-    mbar_init(smem_u32(&s.drain), 1);
+    mbar_init(smem_u32(&s.drain[0]), 1);
+    mbar_init(smem_u32(&s.drain[1]), 1);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -1020,11 +1005,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
     asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
     if (warp == 0) {
       producer_warp<FP8>(s, p, lane, abort);
-    } else if (warp == 1) {
-      if (lane == 0) mma_thread<FP8>(s, tmem, abort);
+    } else if (warp == 1 || warp == 2) {
+      if (lane == 0) mma_thread<FP8>(s, tmem, warp - 1, abort);
       __syncwarp();
     } else if constexpr (FP8) {
-      converter_warps(s, p, threadIdx.x - 64, abort);
+      converter_warp(s, p, lane, abort);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
