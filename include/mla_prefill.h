@@ -112,8 +112,14 @@ mla_status_t mla_prefill_plan(const uint32_t* input_row_offsets, const uint32_t*
  * ceil(total_k_upper_bound / buffer_token_size); 0 if buffer_token_size is 0. */
 uint32_t mla_prefill_plan_max_rows(uint64_t total_k_upper_bound, uint32_t buffer_token_size);
 
-/* Bytes of device workspace mla_prefill_ragged needs for `batch` sequences. */
+/* Bytes of device workspace mla_prefill_ragged needs for `batch` sequences
+ * with bf16 inputs. */
 size_t mla_prefill_ragged_workspace_size(uint32_t batch);
+
+/* Bytes of device workspace mla_prefill_ragged needs with fp8 inputs: the bf16
+ * size plus 128 bytes per K_rope pool slot (pool_slots = num_pages * P), where
+ * each call first writes K_rope converted to bf16 (code * s_r[slot] / s_k). */
+size_t mla_prefill_ragged_workspace_size_fp8(uint32_t batch, uint64_t pool_slots);
 
 /*
  * Ragged MLA prefill attention (flare_mla_prefill: description; Args: output,
@@ -144,16 +150,17 @@ size_t mla_prefill_ragged_workspace_size(uint32_t batch);
  *   row_offsets  device uint32 [B+1], non-decreasing, first entry 0, last = Tq
  *   cache_lens   device uint32 [B]
  *   scale        softmax scale applied to q.k (typically 1/sqrt(192))
- *   workspace    device, >= mla_prefill_ragged_workspace_size(B) bytes,
- *                256-byte aligned; overwritten by every call, so concurrent
- *                calls need distinct workspaces.  Its first uint32 is the
- *                device status word (0 = ok; see mla_read_device_status).
+ *   workspace    device, >= mla_prefill_ragged_workspace_size(B) bytes for bf16
+ *                inputs, >= mla_prefill_ragged_workspace_size_fp8(B, num_pages * P)
+ *                for fp8 inputs; 256-byte aligned; overwritten by every call, so
+ *                concurrent calls need distinct workspaces.  Its first uint32 is
+ *                the device status word (0 = ok; see mla_read_device_status).
  * Shapes, dtypes, strides, alignment and 32-bit index limits are checked on the
  * host.  Offsets and page ids live on the device: an out-of-range page id or
  * page-table column makes the kernel skip that load and set a status bit
  * (MLA_DEVICE_STATUS_*) instead of faulting.
- * Two launches (a one-CTA scheduler, then the persistent attention kernel);
- * no host synchronisation.
+ * Launches: a one-CTA scheduler, for fp8 inputs a K_rope conversion pass, then
+ * the persistent attention kernel; no host synchronisation.
  */
 mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_tensor_t* q,
                                 const mla_tensor_t* k_nope, const mla_tensor_t* v,
@@ -173,7 +180,8 @@ mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_tensor_t* q,
  *   - The scheduler workspace is a fixed device array inside the library
  *     (33,024 bytes, room for 1024 sequences) that every GPU loading the
  *     library keeps until process exit.  A batch above 1024 returns
- *     MLA_ERR_INVALID_ARG.
+ *     MLA_ERR_INVALID_ARG, and so do fp8 inputs, whose K_rope conversion
+ *     needs more room than the array has.
  *   - The first call on a device looks the array's address up with
  *     cudaGetSymbolAddress (one-time set-up with that device current); make
  *     that first call before any stream capture.  Later calls only launch.

@@ -20,8 +20,8 @@ STATUS_BITS = {0x1: "BAD_PAGE", 0x2: "BAD_COLUMN", 0x4: "BAD_OFFSETS", 0x8: "TIM
 
 # Names exported by the C ABI (kept in step with include/mla_prefill.h).
 EXPORTS = ["mla_prefill_plan", "mla_prefill_plan_max_rows", "mla_prefill_ragged_workspace_size",
-           "mla_prefill_ragged", "mla_prefill_ragged_noalloc", "mla_read_device_status",
-           "mla_last_error_string"]
+           "mla_prefill_ragged_workspace_size_fp8", "mla_prefill_ragged", "mla_prefill_ragged_noalloc",
+           "mla_read_device_status", "mla_last_error_string"]
 
 
 class MlaError(RuntimeError):
@@ -54,6 +54,8 @@ def load(path=LIB_PATH):
     lib.mla_prefill_plan_max_rows.restype = u32
     lib.mla_prefill_ragged_workspace_size.argtypes = [u32]
     lib.mla_prefill_ragged_workspace_size.restype = ctypes.c_size_t
+    lib.mla_prefill_ragged_workspace_size_fp8.argtypes = [u32, ctypes.c_uint64]
+    lib.mla_prefill_ragged_workspace_size_fp8.restype = ctypes.c_size_t
     pt = ctypes.POINTER(MlaTensor)
     lib.mla_prefill_ragged.argtypes = [pt, pt, pt, pt, pt, pt, vp, vp, ctypes.c_float, ctypes.c_int,
                                        vp, ctypes.c_size_t, vp]
@@ -132,12 +134,16 @@ def plan(input_row_offsets, cache_lens, buffer_token_size, max_rows, stream=None
     return bro, co, blen, nrows
 
 
-def workspace_size(batch):
+def workspace_size(batch, fp8_pool_slots=None):
+    """Workspace bytes for `batch` sequences; pass the K_rope pool's slot count
+    (num_pages * P) for fp8 inputs."""
+    if fp8_pool_slots is not None:
+        return int(load().mla_prefill_ragged_workspace_size_fp8(int(batch), int(fp8_pool_slots)))
     return int(load().mla_prefill_ragged_workspace_size(int(batch)))
 
 
-def alloc_workspace(batch, device="cuda"):
-    return torch.zeros(workspace_size(batch), dtype=torch.uint8, device=device)
+def alloc_workspace(batch, device="cuda", fp8_pool_slots=None):
+    return torch.zeros(workspace_size(batch, fp8_pool_slots), dtype=torch.uint8, device=device)
 
 
 def prefill_ragged(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens, scale,
@@ -147,9 +153,10 @@ def prefill_ragged(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cac
     the device) and a per-token K_rope scale tensor [num_pages, P]."""
     lib = load()
     B = page_table.shape[0]
-    if workspace is None:
-        workspace = alloc_workspace(B, q.device)
     fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
+    if workspace is None:
+        slots = k_rope_pages.shape[0] * k_rope_pages.shape[1] if fp8 else None
+        workspace = alloc_workspace(B, q.device, slots)
     gran_t = MLA_SCALE_PER_TENSOR if fp8 else MLA_SCALE_NONE
     d_out = describe(out, MLA_DTYPE_BF16)
     d_q = describe(q, _dtype_code(q), q_scale if fp8 else None, gran_t)

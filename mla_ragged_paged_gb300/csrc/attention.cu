@@ -40,6 +40,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -391,8 +392,6 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
   uint32_t recent[C::kRing] = {};    // last group heads issued, for the abort drain
   uint32_t nrecent = 0;
   bool alive = true;
-  // fp8 full barriers count two arrivals (the converter warp adds one to a K group).
-  constexpr int kExtraArrivals = FP8 ? 1 : 0;
 
   auto acquire = [&](uint32_t ps) -> bool {
     return mbar_wait(ring.empty_bar(ps), ring.phase(ps) ^ 1u, abort);
@@ -452,39 +451,33 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     fence_proxy_async_smem();
     __syncwarp();
   };
-  // The K group of tile j: bf16 K_nope[0:64], K_nope[64:128], K_rope at
-  // positions k..k+2; fp8 K_nope at k (the converters fill K_rope at k+1).
+  // The K group of tile j: K_nope chunks (bf16: [0:64] and [64:128] at k,
+  // k+1; fp8: one 128-code chunk at k), then the bf16 K_rope chunk (for fp8
+  // inputs read from the converted copy of the pool).
   auto load_k_group = [&](const ItemInfo& it, int j, uint32_t k) -> bool {
+    constexpr int kNope = FP8 ? 1 : 2;
     const uint32_t bar = ring.full_bar(k);
-    if (FP8) {
-      if (!acquire(k)) return false;
+    const uint32_t kr = k + kNope;  // K_rope slot
+    for (int c = 0; c <= kNope; ++c)
+      if (!acquire(k + c)) return false;
+    if (!p.rope_manual) {
+      uint32_t page = 0, row_in_page = 0;
+      const bool issue = rope_lookup(it, j, page, row_in_page);
+      const uint32_t mask = __ballot_sync(0xffffffffu, issue);
+      const uint32_t bytes = kNope * kChunk + __popc(mask) * p.rope_box * 128u;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar, kChunk);
-        tma_chunk(&p.tm_k, 0, it, j, k, bar);
+        mbar_arrive_expect_tx(bar, bytes);
+        for (int c = 0; c < kNope; ++c) tma_chunk(&p.tm_k, 64 * c, it, j, k + c, bar);
       }
+      __syncwarp();
+      if (issue)
+        tma_load_3d(ring.buf(kr) + lane * p.rope_box * 128u, &p.tm_rope, bar, 0,
+                    static_cast<int>(row_in_page), static_cast<int>(page));
     } else {
-      if (!acquire(k) || !acquire(k + 1) || !acquire(k + 2)) return false;
-      if (!p.rope_manual) {
-        uint32_t page = 0, row_in_page = 0;
-        const bool issue = rope_lookup(it, j, page, row_in_page);
-        const uint32_t mask = __ballot_sync(0xffffffffu, issue);
-        const uint32_t bytes = 2 * kChunk + __popc(mask) * p.rope_box * 128u;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar, bytes);
-          tma_chunk(&p.tm_k, 0, it, j, k, bar);
-          tma_chunk(&p.tm_k, 64, it, j, k + 1, bar);
-        }
-        __syncwarp();
-        if (issue)
-          tma_load_3d(ring.buf(k + 2) + lane * p.rope_box * 128u, &p.tm_rope, bar, 0,
-                      static_cast<int>(row_in_page), static_cast<int>(page));
-      } else {
-        rope_gather(it, j, k + 2);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar, 2 * kChunk);
-          tma_chunk(&p.tm_k, 0, it, j, k, bar);
-          tma_chunk(&p.tm_k, 64, it, j, k + 1, bar);
-        }
+      rope_gather(it, j, kr);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, kNope * kChunk);
+        for (int c = 0; c < kNope; ++c) tma_chunk(&p.tm_k, 64 * c, it, j, k + c, bar);
       }
     }
     note_head(k);
@@ -496,7 +489,6 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     if (!acquire(v) || (!FP8 && !acquire(v + 1))) return false;
     if (lane == 0) {
       mbar_arrive_expect_tx(bar, (FP8 ? 1 : 2) * kChunk);
-      for (int e = 0; e < kExtraArrivals; ++e) mbar_arrive(bar);
       tma_chunk(&p.tm_v, 0, it, j, v, bar);
       if (!FP8) tma_chunk(&p.tm_v, 64, it, j, v + 1, bar);
     }
@@ -559,13 +551,11 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
   }
 }
 
-// fp8 inputs: warp 3 turns the rope parts into bf16 UMMA operands.
-//   Q_rope:  64 e4m3 codes per query row -> bf16 (exact), 128B-swizzled.
-//   K_rope:  per key, the paged pool row (64 codes) times s_r[slot] / s_k,
-//            rounded to bf16, so that q_rope . k_rope' shares the s_q s_k
-//            factor of the nope part.
-// Each lane owns four of the 128 rows; the warp signals the group's mbarrier
-// once its rows are written.
+// fp8 inputs: warp 3 turns each query tile's 64 rope codes per row into
+// bf16 (exact), 128B-swizzled, so q_rope . k_rope' runs as a bf16 UMMA next to
+// the e4m3 nope UMMA.  Each lane owns four of the 128 rows; the warp signals
+// q_full once its rows are written.  (K_rope' = code * s_r[token] / s_k is
+// converted once per call by rope_convert_kernel.)
 __device__ __forceinline__ void store_bf16_row(uint32_t dst, int r, const float (&f)[64]) {
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
@@ -593,19 +583,10 @@ __device__ __forceinline__ void load_e4m3_row(const uint8_t* src, float scale, f
     }
   }
 }
-__device__ void converter_warp(Smem<true>& s, const AttnParams& p, int lane, volatile uint32_t* abort) {
-  using C = Cfg<true>;
-  WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
-  const auto ring = make_ring(s);
-  const float inv_sk = 1.f / *p.k_scale;
-  uint32_t pos = 0, item_k = 0, q_uses[2] = {0, 0}, status = 0;
-  bool alive = true;
 
-  auto signal = [&](uint32_t bar) {
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar);
-  };
+__device__ void converter_warp(Smem<true>& s, const AttnParams& p, int lane, volatile uint32_t* abort) {
+  uint32_t item_k = 0, q_uses[2] = {0, 0};
+  bool alive = true;
   auto conv_q = [&](int q, const ItemInfo& it) -> bool {
     if (!mbar_wait(smem_u32(&s.q_empty[q]), (q_uses[q] & 1u) ^ 1u, abort)) return false;
     ++q_uses[q];
@@ -621,43 +602,38 @@ __device__ void converter_warp(Smem<true>& s, const AttnParams& p, int lane, vol
       }
       store_bf16_row(dst, r, f);
     }
-    signal(smem_u32(&s.q_full[q]));
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.q_full[q]));
     return true;
   };
-  // Tile j's K_rope goes to slot k+1 and completes the K group headed by slot k.
-  auto conv_rope = [&](const ItemInfo& it, int j, uint32_t k) -> bool {
-    if (!mbar_wait(ring.empty_bar(k + 1), ring.phase(k + 1) ^ 1u, abort)) return false;
-    const uint32_t dst = ring.buf(k + 1);
-    for (int r = lane; r < kBN; r += 32) {
-      const int key = j * kBN + r;
-      if (key >= it.L) continue;  // masked keys: stale data is never used
-      const uint32_t col = static_cast<uint32_t>(key) / p.page_size;
-      if (col >= p.max_pages) { status |= MLA_DEVICE_STATUS_BAD_COLUMN; continue; }
-      const uint32_t page = p.page_table[static_cast<long long>(it.b) * p.pt_stride + col];
-      if (page >= p.num_pages) { status |= MLA_DEVICE_STATUS_BAD_PAGE; continue; }
-      const uint32_t in_page = static_cast<uint32_t>(key) - col * p.page_size;
-      const float sc = p.rope_scales[static_cast<long long>(page) * p.page_size + in_page] * inv_sk;
-      float f[64];
-      load_e4m3_row(p.rope_base + page * p.rope_page_bytes + in_page * p.rope_tok_bytes, sc, f);
-      store_bf16_row(dst, r, f);
-    }
-    signal(ring.full_bar(k));
-    return true;
-  };
-
   while (alive) {
     ItemInfo it;
     if (!read_item(s, item_k, lane, it, abort) || !it.valid) break;
-    const int nkv = it.n1 > 0 ? it.nkv1 : it.nkv0;
-    for (int j = 0; j < nkv && alive; ++j) {
-      const TilePos tp = tile_pos<true>(pos);
-      alive = conv_rope(it, j, tp.k);
-      if (alive && j == 0) alive = conv_q(0, it) && (it.n1 == 0 || conv_q(1, it));
-      pos = tp.next;
-    }
-    (void)C::kCPT;
+    alive = conv_q(0, it) && (it.n1 == 0 || conv_q(1, it));
   }
-  if (status) atomicOr(&hdr->status, status);
+}
+
+// fp8 inputs, once per call: K_rope' = e4m3 code * s_r[slot] / s_k in bf16 for
+// every pool slot, into the workspace ([num_pages * P] rows of 64 bf16, 128
+// bytes each).  The attention kernel then streams it like bf16 K_rope.
+__global__ void __launch_bounds__(256) rope_convert_kernel(const uint8_t* __restrict__ pool,
+                                                           long long tok_bytes, long long page_bytes,
+                                                           uint32_t P, uint32_t slots,
+                                                           const float* __restrict__ scales,
+                                                           const float* __restrict__ k_scale,
+                                                           uint16_t* __restrict__ out) {
+  const float inv_sk = 1.f / *k_scale;
+  for (uint32_t sl = blockIdx.x * blockDim.x + threadIdx.x; sl < slots; sl += gridDim.x * blockDim.x) {
+    const uint32_t page = sl / P, row = sl - page * P;
+    float f[64];
+    load_e4m3_row(pool + page * page_bytes + row * tok_bytes, scales[sl] * inv_sk, f);
+    uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(sl) * 64);
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      dst[c] = make_uint4(pack_bf16x2(f[8 * c], f[8 * c + 1]), pack_bf16x2(f[8 * c + 2], f[8 * c + 3]),
+                          pack_bf16x2(f[8 * c + 4], f[8 * c + 5]), pack_bf16x2(f[8 * c + 6], f[8 * c + 7]));
+  }
 }
 
 // UMMA issue for one query tile.  Warps 1 and 2 each run this for their own
@@ -975,10 +951,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
       mbar_init(smem_u32(&s.o_empty[i]), 4);
     }
     for (int i = 0; i < C::kRing; ++i) {
-      // Full barriers are per group (see producer_warp).  fp8: a K group is
-      // completed by the producer's TMA and the converter warp, so every full
-      // barrier takes two arrivals (the producer adds one to V groups).
-      mbar_init(smem_u32(&s.kv_full[i]), FP8 ? 2 : 1);
+      // Full barriers are per group (see producer_warp).
+      mbar_init(smem_u32(&s.kv_full[i]), 1);
       // Both UMMA threads release every chunk.
       mbar_init(smem_u32(&s.kv_empty[i]), 2);
     }
@@ -1049,6 +1023,11 @@ mla_status_t check_tensor(const mla_tensor_t* t, const char* name, int ndim, mla
 extern "C" size_t mla_prefill_ragged_workspace_size(uint32_t batch) {
   size_t bytes = sizeof(mla::WsHeader) + static_cast<size_t>(batch) * sizeof(mla::SeqRec);
   return (bytes + 255) & ~size_t(255);
+}
+
+extern "C" size_t mla_prefill_ragged_workspace_size_fp8(uint32_t batch, uint64_t pool_slots) {
+  // Scheduler records, then the bf16 copy of K_rope' (128 bytes per pool slot).
+  return mla_prefill_ragged_workspace_size(batch) + static_cast<size_t>(pool_slots) * 128;
 }
 
 namespace mla {
@@ -1146,8 +1125,11 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
     return fail(MLA_ERR_INVALID_ARG, "too many work items (query blocks x heads exceeds 2^31)");
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return fail(MLA_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
-  if (workspace_bytes < mla_prefill_ragged_workspace_size(static_cast<uint32_t>(B)))
-    return fail(MLA_ERR_INVALID_ARG, "workspace too small");
+  const size_t ws_need = fp8 ? mla_prefill_ragged_workspace_size_fp8(static_cast<uint32_t>(B),
+                                                                      static_cast<uint64_t>(NP * P))
+                             : mla_prefill_ragged_workspace_size(static_cast<uint32_t>(B));
+  if (workspace_bytes < ws_need)
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes needed", ws_need);
   // TMA and vector-access constraints: 16-byte aligned bases and strides.
   const mla_tensor_t* ts[5] = {q, k_nope, v, k_rope_pages, out};
   const char* names[5] = {"q", "k_nope", "v", "k_rope_pages", "out"};
@@ -1198,14 +1180,24 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
     while (b) { uint32_t t = a % b; a = b; b = t; }
     g = a;  // gcd(P, 128): rows per page segment inside a key tile
   }
-  prm.rope_manual = fp8 || (g % 8u) != 0;
+  prm.rope_manual = (g % 8u) != 0;
   prm.rope_box = g;
+  // bf16 K_rope rows: the caller's pool, or for fp8 inputs the converted copy
+  // the pre-pass writes after the scheduler records in the workspace.
+  void* rope_rows = k_rope_pages->data;
+  uint64_t rope_tok = static_cast<uint64_t>(k_rope_pages->stride[1]) * 2;
+  uint64_t rope_page = static_cast<uint64_t>(k_rope_pages->stride[0]) * 2;
+  if (fp8) {
+    rope_rows = static_cast<uint8_t*>(workspace) + mla_prefill_ragged_workspace_size(static_cast<uint32_t>(B));
+    rope_tok = 128;
+    rope_page = static_cast<uint64_t>(P) * 128;
+  }
   if (!prm.rope_manual) {
     uint64_t dims[3] = {64, (uint64_t)P, (uint64_t)NP};
-    uint64_t str[2] = {(uint64_t)k_rope_pages->stride[1] * 2, (uint64_t)k_rope_pages->stride[0] * 2};
+    uint64_t str[2] = {rope_tok, rope_page};
     uint32_t box[3] = {64, g, 1};
-    if ((st = encode_tiled(&prm.tm_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_rope_pages->data, dims,
-                           str, box, CU_TENSOR_MAP_SWIZZLE_128B, "k_rope_pages")) != MLA_OK)
+    if ((st = encode_tiled(&prm.tm_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rope_rows, dims, str, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "k_rope_pages")) != MLA_OK)
       return st;
   }
   prm.out = static_cast<uint16_t*>(out->data);
@@ -1213,9 +1205,9 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
   prm.out_head = out->stride[1];
   prm.page_table = static_cast<const uint32_t*>(page_table->data);
   prm.pt_stride = page_table->stride[0];
-  prm.rope_base = static_cast<const uint8_t*>(k_rope_pages->data);
-  prm.rope_tok_bytes = k_rope_pages->stride[1] * es;
-  prm.rope_page_bytes = k_rope_pages->stride[0] * es;
+  prm.rope_base = static_cast<const uint8_t*>(rope_rows);
+  prm.rope_tok_bytes = static_cast<long long>(rope_tok);
+  prm.rope_page_bytes = static_cast<long long>(rope_page);
   prm.max_pages = static_cast<uint32_t>(max_pages);
   prm.num_pages = static_cast<uint32_t>(NP);
   prm.page_size = static_cast<uint32_t>(P);
@@ -1232,6 +1224,15 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
     prm.k_scale = k_nope->scale;
     prm.v_scale = v->scale;
     prm.rope_scales = k_rope_pages->scale;
+  }
+  if (fp8) {
+    const uint32_t slots = static_cast<uint32_t>(NP * P);
+    const int blocks = static_cast<int>(std::min<uint32_t>((slots + 255) / 256, 16u * sms));
+    rope_convert_kernel<<<blocks, 256, 0, cs>>>(
+        static_cast<const uint8_t*>(k_rope_pages->data), k_rope_pages->stride[1], k_rope_pages->stride[0],
+        static_cast<uint32_t>(P), slots, k_rope_pages->scale, k_nope->scale, static_cast<uint16_t*>(rope_rows));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "rope conversion launch: %s", cudaGetErrorString(e));
   }
   auto launch = fp8 ? launch_attention<true> : launch_attention<false>;
   return launch(prm, dev, sms, row_offsets, cache_lens, static_cast<uint32_t>(B), static_cast<uint32_t>(H),

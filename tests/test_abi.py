@@ -44,6 +44,7 @@ def test_host_helpers(lib):
     assert binding.plan_max_rows(10, 0) == 0
     ws = binding.workspace_size(8)
     assert ws % 256 == 0 and ws >= 256 + 8 * 32
+    assert binding.workspace_size(8, fp8_pool_slots=1000) == ws + 1000 * 128
 
 
 def _desc(shape, dtype=binding.MLA_DTYPE_BF16, ptr=0x10000):

@@ -25,7 +25,8 @@ def run_gpu(w, workspace=None):
     d = workloads.device_inputs(w)
     out = torch.full((w.total_q, w.heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
     pool = d["k_rope_pool"][..., w.spec.rope_col:w.spec.rope_col + 64]
-    ws = binding.alloc_workspace(w.batch) if workspace is None else workspace
+    slots = w.num_pages * w.page_size if w.spec.dtype == "fp8" else None
+    ws = binding.alloc_workspace(w.batch, fp8_pool_slots=slots) if workspace is None else workspace
     mask = binding.MLA_MASK_CAUSAL if w.spec.mask == "causal" else binding.MLA_MASK_NULL
     binding.prefill_ragged(out, d["q"], d["k_nope"], d["v"], pool, d["page_table"],
                            d["row_offsets"], d["cache_lens"], w.scale, mask, ws,
