@@ -38,9 +38,10 @@ METRIC = "MLA prefill causal-effective TFLOP/s and % of GB300 tensor peak, 1 GPU
 WORKLOAD = "deepseek_v3_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic of one attention launch on this workload, from the ncu capture
+# DRAM traffic of one attention launch per workload, from the ncu captures
 # summarised in profiles/; valid only while the kernel source is unchanged.
-ATTENTION_TRAFFIC = {"source_sha1": "1d2b22b17a6effd2e8bd40089901be5931b98f2d", "bytes_per_launch": 2399135000}
+ATTENTION_TRAFFIC = {"source_sha1": "2a1b323e7a75ac39a00403dca8e5e2e0673651ea",
+                     "bytes_per_launch": {"deepseek_v3_bf16": 2389273000, "fp8_e4m3": 3186384000}}
 
 
 def causal_flops(w):
@@ -185,7 +186,7 @@ def host_cores():
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    w = workloads.generate(workloads.config(WORKLOAD))
+    w = workloads.generate(workloads.config(args.workload))
     per_step = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
     rows, nh = oracle_shape_for(w, per_step)
     for i in range(args.warmup):
@@ -200,7 +201,7 @@ def run_reference(args, world, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample_per_step": "query rows of one (sequence, head)"},
+            "config": {"workload": args.workload, "sample_per_step": "query rows of one (sequence, head)"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(),
                              "kind": "oracle", "sample": f"per step: {sample}"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -216,6 +217,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=[c.name for c in workloads.CONFIGS],
+                    help="workload to time (default: the DeepSeek-V3-shaped bf16 batch)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -231,15 +234,18 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    spec = workloads.config(WORKLOAD)
+    spec = workloads.config(args.workload)
+    fp8 = spec.dtype == "fp8"
     w = workloads.generate(spec if rank == 0 else replace(spec, seed=spec.seed + 1000 * rank))
     F = causal_flops(w)
     d = workloads.device_inputs(w, device=dev)
+    in_bytes = sum(t.numel() * t.element_size() for t in d.values())
     Tq, H, B = w.total_q, w.heads, w.batch
     T = spec.buffer_token_size
     R = (w.total_k + T - 1) // T
     out = torch.empty((Tq, H, 128), dtype=torch.bfloat16, device=dev)
-    ws = binding.alloc_workspace(B, dev)
+    ws = binding.alloc_workspace(B, dev, fp8_pool_slots=w.num_pages * w.page_size if fp8 else None)
+    scales = {k: d.get(k) for k in ("q_scale", "k_scale", "v_scale", "k_rope_scales")}
     plan_out = (torch.empty((R, B + 1), dtype=torch.int32, device=dev),
                 torch.empty((R, B), dtype=torch.int32, device=dev),
                 torch.empty((R,), dtype=torch.int32, device=dev),
@@ -250,7 +256,7 @@ def main():
         binding.plan(inp["row_offsets"], inp["cache_lens"], T, R, stream=stream, out=plan_out)
         binding.prefill_ragged(o, inp["q"], inp["k_nope"], inp["v"], inp["k_rope_pool"],
                                inp["page_table"], inp["row_offsets"], inp["cache_lens"], w.scale,
-                               binding.MLA_MASK_CAUSAL, ws, stream=stream)
+                               binding.MLA_MASK_CAUSAL, ws, stream=stream, **scales)
 
     for _ in range(args.warmup):
         step(d, out)
@@ -271,7 +277,7 @@ def main():
             ev[i][1].record(stream)
             binding.prefill_ragged(out, d["q"], d["k_nope"], d["v"], d["k_rope_pool"],
                                    d["page_table"], d["row_offsets"], d["cache_lens"], w.scale,
-                                   binding.MLA_MASK_CAUSAL, ws, stream=stream)
+                                   binding.MLA_MASK_CAUSAL, ws, stream=stream, **scales)
             ev[i][2].record(stream)
         t_end.record(stream)
         barrier(world)
@@ -284,6 +290,8 @@ def main():
     # attention, output -> pinned host, every step.
     h = workloads.device_inputs(w, device="cpu", pin=True)
     keys = ["q", "k_nope", "v", "k_rope_pool", "page_table", "row_offsets", "cache_lens"]
+    if fp8:
+        keys += ["q_scale", "k_scale", "v_scale", "k_rope_scales"]
     d2 = {k: torch.empty_like(d[k]) for k in keys}
     out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(h[k].numel() * h[k].element_size() for k in keys)
@@ -292,6 +300,8 @@ def main():
     def e2e_step():
         for k in keys:
             d2[k].copy_(h[k], non_blocking=True)
+        if fp8:
+            scales.update({k: d2[k] for k in ("q_scale", "k_scale", "v_scale", "k_rope_scales")})
         step(d2, out)
         out_host.copy_(out, non_blocking=True)
 
@@ -308,11 +318,12 @@ def main():
     e2e_ms = dist_max(e0.elapsed_time(e1), world)
 
     peaks, peak_src = load_peaks()
-    peak = peaks["bf16_tflops"]
+    # fp8 UMMAs run at twice the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s dense).
+    peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
     achieved = F / (attn_ms * 1e-3) / 1e12
     traffic = None
     if ATTENTION_TRAFFIC["source_sha1"] == source_sha1():
-        traffic = ATTENTION_TRAFFIC["bytes_per_launch"]
+        traffic = ATTENTION_TRAFFIC["bytes_per_launch"].get(spec.name)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -326,22 +337,22 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if fp8 else "bf16",
             "data": "synthetic",
-            "config": {"workload": f"{WORKLOAD}: {spec.description}", "global_batch": B * world,
+            "config": {"workload": f"{spec.name}: {spec.description}", "global_batch": B * world,
                        "total_q_tokens": Tq, "heads": H, "causal_effective_tflop_per_step": F / 1e12,
                        "parallelism": f"dp{world} (independent batches)" if world > 1 else "none",
-                       "l2": "inputs (2.1 GB) larger than L2; no flush",
+                       "l2": f"inputs ({in_bytes / 1e9:.2f} GB) larger than L2; no flush",
                        "step": "mla_prefill_plan + mla_prefill_ragged"},
             "pct_of_peak": 100.0 * value / world / peak,
             "clocks": clocks,
             "e2e": {"value": world * F * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": (4 if fp8 else 3) * args.steps,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                          "kernel": "mla_attention_kernel (+ its 1-CTA scheduler launch in the span)",
-                         "peak_source": f"{peak_src} bf16_tflops (burst)"},
+                         "peak_source": f"{peak_src} bf16_tflops (burst)" + (" x 2 (fp8/bf16 nominal ratio)" if fp8 else "")},
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
