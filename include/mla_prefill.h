@@ -8,6 +8,8 @@
  *   mla_prefill_ragged  ragged causal attention with a 192-wide Q head, 128
  *                       per-head K_nope dims plus 64 K_rope dims shared by all
  *                       heads, 128-wide V and output (flare_mla_prefill).
+ * Chunked execution runs the second stage once per buffer row of the plan
+ * (mla_prefill_ragged_chunk) and combines the rows (mla_prefill_merge).
  *
  * Conventions shared by every entry point:
  *   - Every pointer marked "device" is caller-owned device memory; the library
@@ -45,6 +47,7 @@ typedef enum {
   MLA_DTYPE_BF16 = 0,
   MLA_DTYPE_FP8_E4M3 = 1, /* float8_e4m3fn: no infinities, 0x7F/0xFF are NaN */
   MLA_DTYPE_U32 = 2,
+  MLA_DTYPE_F32 = 3,
 } mla_dtype_t;
 
 typedef enum {
@@ -198,6 +201,66 @@ mla_status_t mla_prefill_ragged_noalloc(const mla_tensor_t* out, const mla_tenso
                                         const mla_tensor_t* page_table,
                                         const uint32_t* row_offsets, const uint32_t* cache_lens,
                                         float scale, mla_mask_t mask, mla_stream_t stream);
+
+/*
+ * One buffer row of chunked execution (flare_mla_prefill: Args
+ * cache_row_offsets, cache_offsets; generic_flare_mla_prefill_ragged_paged_plan:
+ * buffer_row_offsets, cache_offsets, buffer_lengths).
+ *
+ * The plan cuts the K context into buffer rows; row r holds, for sequence b,
+ * W_b = buffer_row_offsets[b+1] - buffer_row_offsets[b] keys, the context
+ * positions a = cache_offsets[b] .. cache_offsets[b] + W_b - 1, at rows
+ * buffer_row_offsets[b] + (a - cache_offsets[b]) of this call's k_nope / v
+ * (the row's contiguous K buffer).  Pass row r of the plan's outputs:
+ * buffer_row_offsets + r * (B + 1) and cache_offsets + r * B.  Everything
+ * else is as in mla_prefill_ragged, with these differences:
+ *   - keys are the row's only; the causal mask and the K_rope page lookup use
+ *     the context position a (causal: a <= cache_lens[b] + i);
+ *   - out receives the softmax over the row's visible keys, and
+ *     lse[t, h] = ln sum_j exp(s_j) over the same keys (natural log, s_j the
+ *     scaled scores; fp8 scores include the dequantisation scales);
+ *   - a query that sees no key of the row gets out = 0 and lse = -inf;
+ *   - rows of sequences with W_b = 0 are not written (neither out nor lse).
+ *   lse          device float32 [Tq, H] (written), 4-byte aligned
+ *   k_nope, v    device [S_row, H, 128] with S_row >= buffer_row_offsets[B] >= 1
+ *   buffer_row_offsets  device uint32 [B+1], non-decreasing
+ *   cache_offsets       device uint32 [B]; cache_offsets[b] + W_b <= L_b
+ * A window outside a sequence's context sets MLA_DEVICE_STATUS_BAD_OFFSETS
+ * and skips that sequence.  Workspace sizes and launches are those of
+ * mla_prefill_ragged.
+ */
+mla_status_t mla_prefill_ragged_chunk(const mla_tensor_t* out, const mla_tensor_t* lse,
+                                      const mla_tensor_t* q, const mla_tensor_t* k_nope,
+                                      const mla_tensor_t* v, const mla_tensor_t* k_rope_pages,
+                                      const mla_tensor_t* page_table, const uint32_t* row_offsets,
+                                      const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
+                                      const uint32_t* cache_offsets, float scale, mla_mask_t mask,
+                                      void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * Combines the rows of a chunked execution (the pages give only the per-row
+ * call; the combination is the standard log-sum-exp weighting).  For each
+ * token t of sequence b and head h, over the rows r whose window holds keys of
+ * b (buffer_row_offsets[r, b+1] > buffer_row_offsets[r, b]) and whose
+ * lse_r = partial_lse[r, t, h] is finite:
+ *   out[t, h, :] = sum_r e^(lse_r - m) partial_out[r, t, h, :] / sum_r e^(lse_r - m),
+ *   m = max_r lse_r;  0 when no row qualifies.
+ *   out                 device bf16 [Tq, H, 128] (written for tokens
+ *                       row_offsets[0] .. row_offsets[B]-1 only), 16-byte
+ *                       aligned rows
+ *   partial_out         device bf16 [R, Tq, H, 128], as written by
+ *                       mla_prefill_ragged_chunk for rows 0..R-1
+ *   partial_lse         device float32 [R, Tq, H]
+ *   row_offsets         device uint32 [B+1] (the attention calls' Q offsets)
+ *   buffer_row_offsets  device uint32, row r at buffer_row_offsets + r * (B+1)
+ *                       (the plan's output), rows 0..R-1 read
+ *   batch               B >= 1
+ * One launch, no host synchronisation.
+ */
+mla_status_t mla_prefill_merge(const mla_tensor_t* out, const mla_tensor_t* partial_out,
+                               const mla_tensor_t* partial_lse, const uint32_t* row_offsets,
+                               const uint32_t* buffer_row_offsets, uint32_t batch,
+                               mla_stream_t stream);
 
 /* Device status bits written into the workspace's first uint32. */
 #define MLA_DEVICE_STATUS_BAD_PAGE 0x1u    /* page id >= num_pages */

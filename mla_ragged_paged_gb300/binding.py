@@ -13,7 +13,7 @@ import torch
 from .buildlib import LIB_PATH
 
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, 1, 2, 3
-MLA_DTYPE_BF16, MLA_DTYPE_FP8_E4M3, MLA_DTYPE_U32 = 0, 1, 2
+MLA_DTYPE_BF16, MLA_DTYPE_FP8_E4M3, MLA_DTYPE_U32, MLA_DTYPE_F32 = 0, 1, 2, 3
 MLA_MASK_CAUSAL, MLA_MASK_NULL = 0, 1
 MLA_SCALE_NONE, MLA_SCALE_PER_TENSOR, MLA_SCALE_PER_TOKEN = 0, 1, 2
 STATUS_BITS = {0x1: "BAD_PAGE", 0x2: "BAD_COLUMN", 0x4: "BAD_OFFSETS", 0x8: "TIMEOUT"}
@@ -21,7 +21,8 @@ STATUS_BITS = {0x1: "BAD_PAGE", 0x2: "BAD_COLUMN", 0x4: "BAD_OFFSETS", 0x8: "TIM
 # Names exported by the C ABI (kept in step with include/mla_prefill.h).
 EXPORTS = ["mla_prefill_plan", "mla_prefill_plan_max_rows", "mla_prefill_ragged_workspace_size",
            "mla_prefill_ragged_workspace_size_fp8", "mla_prefill_ragged", "mla_prefill_ragged_noalloc",
-           "mla_read_device_status", "mla_last_error_string"]
+           "mla_prefill_ragged_chunk", "mla_prefill_merge", "mla_read_device_status",
+           "mla_last_error_string"]
 
 
 class MlaError(RuntimeError):
@@ -63,6 +64,11 @@ def load(path=LIB_PATH):
     lib.mla_prefill_ragged_noalloc.argtypes = [pt, pt, pt, pt, pt, pt, vp, vp, ctypes.c_float,
                                                ctypes.c_int, vp]
     lib.mla_prefill_ragged_noalloc.restype = ctypes.c_int
+    lib.mla_prefill_ragged_chunk.argtypes = [pt, pt, pt, pt, pt, pt, pt, vp, vp, vp, vp, ctypes.c_float,
+                                             ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.mla_prefill_ragged_chunk.restype = ctypes.c_int
+    lib.mla_prefill_merge.argtypes = [pt, pt, pt, vp, vp, u32, vp]
+    lib.mla_prefill_merge.restype = ctypes.c_int
     lib.mla_read_device_status.argtypes = [vp, ctypes.POINTER(u32), vp]
     lib.mla_read_device_status.restype = ctypes.c_int
     lib.mla_last_error_string.argtypes = []
@@ -107,6 +113,8 @@ def _dtype_code(t):
         return MLA_DTYPE_FP8_E4M3
     if t.dtype in (torch.int32,) or str(t.dtype) == "torch.uint32":
         return MLA_DTYPE_U32
+    if t.dtype == torch.float32:
+        return MLA_DTYPE_F32
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
@@ -170,6 +178,90 @@ def prefill_ragged(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cac
                                   _ptr(row_offsets), _ptr(cache_lens), float(scale), int(mask),
                                   _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
+
+
+def _inputs(q, k_nope, v, k_rope_pages, page_table, q_scale, k_scale, v_scale, k_rope_scales):
+    fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
+    gran_t = MLA_SCALE_PER_TENSOR if fp8 else MLA_SCALE_NONE
+    return (describe(q, _dtype_code(q), q_scale if fp8 else None, gran_t),
+            describe(k_nope, _dtype_code(k_nope), k_scale if fp8 else None, gran_t),
+            describe(v, _dtype_code(v), v_scale if fp8 else None, gran_t),
+            describe(k_rope_pages, _dtype_code(k_rope_pages), k_rope_scales if fp8 else None,
+                     MLA_SCALE_PER_TOKEN if fp8 else MLA_SCALE_NONE),
+            describe(page_table, MLA_DTYPE_U32))
+
+
+def prefill_ragged_chunk(out, lse, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,
+                         buffer_row_offsets, cache_offsets, scale, mask=MLA_MASK_CAUSAL,
+                         workspace=None, q_scale=None, k_scale=None, v_scale=None, k_rope_scales=None,
+                         stream=None):
+    """mla_prefill_ragged_chunk: one buffer row.  k_nope / v are the row's K
+    buffer; buffer_row_offsets [B+1] and cache_offsets [B] are that row of the
+    plan (device int32 views of the uint32 values); lse is float32 [Tq, H]."""
+    lib = load()
+    B = page_table.shape[0]
+    fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
+    if workspace is None:
+        slots = k_rope_pages.shape[0] * k_rope_pages.shape[1] if fp8 else None
+        workspace = alloc_workspace(B, q.device, slots)
+    d_q, d_k, d_v, d_r, d_pt = _inputs(q, k_nope, v, k_rope_pages, page_table, q_scale, k_scale,
+                                       v_scale, k_rope_scales)
+    d_out = describe(out, MLA_DTYPE_BF16)
+    d_lse = describe(lse, MLA_DTYPE_F32)
+    _check(lib.mla_prefill_ragged_chunk(ctypes.byref(d_out), ctypes.byref(d_lse), ctypes.byref(d_q),
+                                        ctypes.byref(d_k), ctypes.byref(d_v), ctypes.byref(d_r),
+                                        ctypes.byref(d_pt), _ptr(row_offsets), _ptr(cache_lens),
+                                        _ptr(buffer_row_offsets), _ptr(cache_offsets), float(scale),
+                                        int(mask), _ptr(workspace), workspace.numel(),
+                                        _stream(stream)))
+    return out, lse
+
+
+def merge(out, partial_out, partial_lse, row_offsets, buffer_row_offsets, stream=None):
+    """mla_prefill_merge over rows 0..R-1 (R = partial_out.shape[0]);
+    buffer_row_offsets is the plan's [R_max, B+1] array."""
+    B = row_offsets.numel() - 1
+    assert buffer_row_offsets.shape[-1] == B + 1 and buffer_row_offsets.stride(0) == B + 1
+    d_out = describe(out, MLA_DTYPE_BF16)
+    d_po = describe(partial_out, MLA_DTYPE_BF16)
+    d_pl = describe(partial_lse, MLA_DTYPE_F32)
+    _check(load().mla_prefill_merge(ctypes.byref(d_out), ctypes.byref(d_po), ctypes.byref(d_pl),
+                                    _ptr(row_offsets), _ptr(buffer_row_offsets), B, _stream(stream)))
+    return out
+
+
+def chunked_scratch(num_rows, total_q, heads, device="cuda"):
+    """Per-row partial outputs [R, Tq, H, 128] bf16 and lse [R, Tq, H] float32."""
+    return (torch.empty((num_rows, total_q, heads, 128), dtype=torch.bfloat16, device=device),
+            torch.empty((num_rows, total_q, heads), dtype=torch.float32, device=device))
+
+
+def prefill_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens, scale,
+                    buffer_token_size, total_k, mask=MLA_MASK_CAUSAL, workspace=None, scratch=None,
+                    q_scale=None, k_scale=None, v_scale=None, k_rope_scales=None, stream=None):
+    """Chunked execution: the plan, one mla_prefill_ragged_chunk per buffer
+    row, then mla_prefill_merge.  k_nope / v hold the contexts packed in batch
+    order (the full-context layout), so buffer row r's K buffer is rows
+    r*T .. r*T + T - 1 of them.  total_k (host int) is the number of context
+    tokens, sum of (new + cached) lengths, which fixes the row count."""
+    T = int(buffer_token_size)
+    R = max(1, -(-int(total_k) // T))
+    B = page_table.shape[0]
+    fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
+    if workspace is None:
+        slots = k_rope_pages.shape[0] * k_rope_pages.shape[1] if fp8 else None
+        workspace = alloc_workspace(B, q.device, slots)
+    if scratch is None:
+        scratch = chunked_scratch(R, q.shape[0], q.shape[1], q.device)
+    po, pl = scratch
+    bro, co, _, _ = plan(row_offsets, cache_lens, T, R, stream=stream)
+    Sk = k_nope.shape[0]
+    for r in range(R):
+        lo, hi = r * T, min((r + 1) * T, Sk)
+        prefill_ragged_chunk(po[r], pl[r], q, k_nope[lo:hi], v[lo:hi], k_rope_pages, page_table,
+                             row_offsets, cache_lens, bro[r], co[r], scale, mask, workspace,
+                             q_scale, k_scale, v_scale, k_rope_scales, stream)
+    return merge(out, po[:R], pl[:R], row_offsets, bro, stream)
 
 
 def prefill_ragged_noalloc(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,

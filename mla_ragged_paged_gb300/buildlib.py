@@ -18,7 +18,7 @@ LIB_NAME = "libmla_prefill.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 BUILD_DIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["host_common.cpp", "plan.cu", "attention.cu"]
+SOURCES = ["host_common.cpp", "plan.cu", "attention.cu", "merge.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
          "-diag-suppress", "177"]

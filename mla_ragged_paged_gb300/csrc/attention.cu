@@ -86,13 +86,17 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header");
 
-// One sequence, in scheduling order.
+// One sequence, in scheduling order.  Its keys are the window of W context
+// positions starting at co (the whole context, co = 0, for a full-context
+// call; one buffer row's share for a chunked call), held at K/V rows
+// kv_start .. kv_start + W - 1.  bg = b | (head group size << 16).
 struct SeqRec {
-  uint32_t q_start, n, prior, kv_start, b, nqb, group, item_start;
+  uint32_t q_start, n, prior, kv_start, bg, item_start, W, co;
 };
 
+// shift = prior - co: window key j is visible to query i when j <= shift + i.
 struct ItemInfo {
-  int32_t valid, b, h, q_row0, i0, n, prior, L, kv_row0, n0, n1, nkv0, nkv1, pad[3];
+  int32_t valid, b, h, q_row0, i0, n, shift, W, kv_row0, n0, n1, nkv0, nkv1, co, pad[2];
 };
 
 struct AttnParams {
@@ -102,6 +106,8 @@ struct AttnParams {
   CUtensorMap tm_rope;
   uint16_t* out;
   long long out_tok, out_head;
+  float* lse;                 // chunked calls: [Tq, H] natural-log sum of exp(scores), else NULL
+  long long lse_tok, lse_head;
   const uint32_t* page_table;
   long long pt_stride;
   const uint8_t* rope_base;
@@ -177,12 +183,13 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* warp_t
 }
 
 __global__ void __launch_bounds__(kSchedThreads, 1)
-schedule_kernel(const uint32_t* __restrict__ ro, const uint32_t* __restrict__ cl, uint32_t B,
+schedule_kernel(const uint32_t* __restrict__ ro, const uint32_t* __restrict__ cl,
+                const uint32_t* __restrict__ bro, const uint32_t* __restrict__ cof, uint32_t B,
                 uint32_t H, uint32_t Tq, uint32_t Sk, uint32_t P, uint32_t max_pages,
                 uint32_t kv_bytes_per_key_head, uint8_t* __restrict__ ws) {
   extern __shared__ uint32_t sm[];
   uint32_t* kv_start = sm;           // [B]
-  uint32_t* key = sm + B;            // [B]  context length (0 = no work)
+  uint32_t* key = sm + B;            // [B]  keys in the window (0 = no work)
   uint32_t* order = sm + 2 * B;      // [B]  scheduling position -> sequence
   __shared__ uint32_t warp_tot[32];
   __shared__ uint32_t total_s;
@@ -207,16 +214,30 @@ schedule_kernel(const uint32_t* __restrict__ ro, const uint32_t* __restrict__ cl
     const uint32_t lo = ro[b], hi = ro[b + 1];
     const uint32_t n = hi >= lo ? hi - lo : 0u;
     const uint64_t L = static_cast<uint64_t>(cl[b]) + n;
-    uint32_t k = static_cast<uint32_t>(L);
-    if (hi < lo || hi > Tq || static_cast<uint64_t>(run) + L > Sk) {
+    // Window: the whole context at K rows run.., or (chunked call) the
+    // buffer row's W keys from context position co at rows bro[b]...
+    uint64_t w0 = 0, W = L, start = run;
+    bool ok = hi >= lo && hi <= Tq && L <= 0x7FFFFFFFull;
+    if (bro) {
+      const uint32_t r0 = bro[b], r1 = bro[b + 1];
+      ok = ok && r0 <= r1 && r1 <= Sk;
+      w0 = cof[b];
+      W = r1 >= r0 ? r1 - r0 : 0u;
+      start = r0;
+      ok = ok && w0 + W <= L;
+    } else {
+      ok = ok && static_cast<uint64_t>(run) + L <= Sk;
+    }
+    uint32_t k = static_cast<uint32_t>(W);
+    if (!ok) {
       bad |= MLA_DEVICE_STATUS_BAD_OFFSETS;
       k = 0;
-    } else if ((L + P - 1) / P > max_pages) {
+    } else if ((w0 + W + P - 1) / P > max_pages) {
       bad |= MLA_DEVICE_STATUS_BAD_COLUMN;
       k = 0;
     }
     if (n == 0) k = 0;
-    kv_start[b] = run;
+    kv_start[b] = static_cast<uint32_t>(start);
     key[b] = k;
     run += static_cast<uint32_t>(min(L, static_cast<uint64_t>(0x7FFFFFFFu)));
   }
@@ -250,20 +271,21 @@ schedule_kernel(const uint32_t* __restrict__ ro, const uint32_t* __restrict__ cl
   for (uint32_t s = b0; s < b1; ++s) {
     const uint32_t b = order[s];
     SeqRec r;
-    r.b = b;
     r.q_start = ro[b];
     r.n = key[b] ? ro[b + 1] - ro[b] : 0u;
     r.prior = cl[b];
     r.kv_start = kv_start[b];
-    r.nqb = (r.n + kQRows - 1) / kQRows;
+    r.W = key[b];
+    r.co = bro ? cof[b] : 0u;
     const uint64_t head_bytes = static_cast<uint64_t>(key[b]) * kv_bytes_per_key_head;
     uint64_t g = head_bytes ? kL2GroupBytes / head_bytes : H;
     if (g > H) g = H;
+    if (g > 0xFFFF) g = 0xFFFF;
     if (g < 1) g = 1;
-    r.group = static_cast<uint32_t>(g);
+    r.bg = b | (static_cast<uint32_t>(g) << 16);
     r.item_start = item;
     recs[s] = r;
-    item += r.nqb * H;
+    item += ((r.n + kQRows - 1) / kQRows) * H;
   }
   if (tid == 0) {
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
@@ -288,28 +310,32 @@ __device__ __forceinline__ ItemInfo decode_item(uint32_t t, const WsHeader* hdr,
     if (recs[mid].item_start <= t) lo = mid; else hi = mid;
   }
   const SeqRec r = recs[lo];
+  const uint32_t nqb = (r.n + kQRows - 1) / kQRows;
   const uint32_t u = t - r.item_start;
-  const uint32_t G = r.group;
-  const uint32_t g = u / (r.nqb * G);
-  const uint32_t rem = u - g * r.nqb * G;
+  const uint32_t G = r.bg >> 16;
+  const uint32_t g = u / (nqb * G);
+  const uint32_t rem = u - g * nqb * G;
   const uint32_t Gg = min(G, H - g * G);
   const uint32_t qrev = rem / Gg;
   const uint32_t hh = rem - qrev * Gg;
-  const int qblk = static_cast<int>(r.nqb - 1 - qrev);
+  const int qblk = static_cast<int>(nqb - 1 - qrev);
   it.valid = 1;
-  it.b = static_cast<int>(r.b);
+  it.b = static_cast<int>(r.bg & 0xFFFFu);
   it.h = static_cast<int>(g * G + hh);
   it.n = static_cast<int>(r.n);
-  it.prior = static_cast<int>(r.prior);
-  it.L = it.n + it.prior;
+  it.shift = static_cast<int>(r.prior) - static_cast<int>(r.co);
+  it.W = static_cast<int>(r.W);
+  it.co = static_cast<int>(r.co);
   it.i0 = qblk * kQRows;
   it.q_row0 = static_cast<int>(r.q_start) + it.i0;
   it.kv_row0 = static_cast<int>(r.kv_start);
   it.n0 = min(kBM, it.n - it.i0);
   it.n1 = max(0, min(kBM, it.n - it.i0 - kBM));
-  const int all_tiles = (it.L + kBN - 1) / kBN;
-  it.nkv0 = causal ? (it.prior + it.i0 + it.n0 - 1) / kBN + 1 : all_tiles;
-  it.nkv1 = it.n1 > 0 ? (causal ? (it.prior + it.i0 + kBM + it.n1 - 1) / kBN + 1 : all_tiles) : 0;
+  // KV tiles up to the one holding window key `last` (none if last < 0).
+  const int all_tiles = (it.W + kBN - 1) / kBN;
+  auto tiles = [&](int last) { return last < 0 ? 0 : min(last / kBN + 1, all_tiles); };
+  it.nkv0 = causal ? tiles(it.shift + it.i0 + it.n0 - 1) : all_tiles;
+  it.nkv1 = it.n1 > 0 ? (causal ? tiles(it.shift + it.i0 + kBM + it.n1 - 1) : all_tiles) : 0;
   return it;
 }
 
@@ -406,16 +432,17 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     tma_load_3d(ring.buf(ps), map, bar, x, it.h, it.kv_row0 + j * kBN);
   };
   // bf16 K_rope rows into slot `ps`: TMA boxes (one per page segment, lane t
-  // owns box t) when pages are 8-row aligned, else a swizzled row gather.
-  // Returns the bytes the TMA boxes will deliver (0 for the gather).
+  // owns box t) when page segments are 8-row aligned, else a swizzled row
+  // gather.  Window key `key` is context position co + key.
   auto rope_lookup = [&](const ItemInfo& it, int j, uint32_t& page, uint32_t& row_in_page) -> bool {
     const int nbox = kBN / static_cast<int>(p.rope_box);
     bool issue = false;
     if (lane < nbox) {
       const int key = j * kBN + lane * static_cast<int>(p.rope_box);
-      if (key < it.L) {
-        const uint32_t col = static_cast<uint32_t>(key) / p.page_size;
-        row_in_page = static_cast<uint32_t>(key) - col * p.page_size;
+      if (key < it.W) {
+        const uint32_t a = static_cast<uint32_t>(it.co + key);
+        const uint32_t col = a / p.page_size;
+        row_in_page = a - col * p.page_size;
         if (col >= p.max_pages) {
           status |= MLA_DEVICE_STATUS_BAD_COLUMN;
         } else {
@@ -431,14 +458,15 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     const uint32_t dst = ring.buf(ps);
     for (int r = lane; r < kBN; r += 32) {
       const int key = j * kBN + r;
-      if (key >= it.L) continue;
-      const uint32_t col = static_cast<uint32_t>(key) / p.page_size;
+      if (key >= it.W) continue;
+      const uint32_t a = static_cast<uint32_t>(it.co + key);
+      const uint32_t col = a / p.page_size;
       if (col >= p.max_pages) { status |= MLA_DEVICE_STATUS_BAD_COLUMN; continue; }
       const uint32_t page = p.page_table[static_cast<long long>(it.b) * p.pt_stride + col];
       if (page >= p.num_pages) { status |= MLA_DEVICE_STATUS_BAD_PAGE; continue; }
       const uint4* src = reinterpret_cast<const uint4*>(
           p.rope_base + page * p.rope_page_bytes +
-          static_cast<long long>(key - static_cast<int>(col * p.page_size)) * p.rope_tok_bytes);
+          static_cast<long long>(a - col * p.page_size) * p.rope_tok_bytes);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const uint4 v = src[c];
@@ -460,7 +488,8 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     const uint32_t kr = k + kNope;  // K_rope slot
     for (int c = 0; c <= kNope; ++c)
       if (!acquire(k + c)) return false;
-    if (!p.rope_manual) {
+    // A window that starts inside a page segment takes the row gather.
+    if (!p.rope_manual && it.co % static_cast<int>(p.rope_box) == 0) {
       uint32_t page = 0, row_in_page = 0;
       const bool issue = rope_lookup(it, j, page, row_in_page);
       const uint32_t mask = __ballot_sync(0xffffffffu, issue);
@@ -526,7 +555,8 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     for (int j = 0; j < nkv && alive; ++j) {
       const TilePos tp = tile_pos<FP8>(pos);
       alive = load_k_group(it, j, tp.k);
-      if (alive && j == 0) alive = load_q(0, it) && (it.n1 == 0 || load_q(1, it));
+      // A query tile that sees no key of the window is not loaded.
+      if (alive && j == 0) alive = (it.nkv0 == 0 || load_q(0, it)) && (it.nkv1 == 0 || load_q(1, it));
       if (alive && tp.pad != kNoPad) {  // pad slot: keeps the V pair adjacent
         alive = acquire(tp.pad);
         if (alive) {
@@ -610,7 +640,7 @@ __device__ void converter_warp(Smem<true>& s, const AttnParams& p, int lane, vol
   while (alive) {
     ItemInfo it;
     if (!read_item(s, item_k, lane, it, abort) || !it.valid) break;
-    alive = conv_q(0, it) && (it.n1 == 0 || conv_q(1, it));
+    alive = (it.nkv0 == 0 || conv_q(0, it)) && (it.nkv1 == 0 || conv_q(1, it));
   }
 }
 
@@ -727,6 +757,7 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
     ++item_k;
     if (!it.valid) break;
     const int nkv = it.n1 > 0 ? it.nkv1 : it.nkv0;   // KV tiles the item streams
+    if (nkv == 0) continue;                           // no query of the item sees a key
     const int mine = q ? (it.n1 > 0 ? it.nkv1 : 0) : it.nkv0;  // tiles this query tile uses
     TilePos cur = tile_pos<FP8>(pos);
     alive = wait_group(cur.k);
@@ -792,9 +823,20 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
     if (q == 1 && it.n1 == 0) continue;
     const int nkv = q ? it.nkv1 : it.nkv0;
     const int i = it.i0 + q * kBM + r;  // query index inside the sequence
-    const int last_key = it.L - 1;
-    const int limit = p.causal ? min(it.prior + i, last_key) : last_key;
-    const int tile_limit = p.causal ? min(it.prior + it.i0 + q * kBM, last_key) : last_key;
+    if (nkv == 0) {
+      // Chunked call, no query of this tile sees a key of the window.
+      if (i < it.n) {
+        const long long row = it.q_row0 + q * kBM + r;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.out_tok + static_cast<long long>(it.h) * p.out_head);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        if (p.lse) p.lse[row * p.lse_tok + static_cast<long long>(it.h) * p.lse_head] = -INFINITY;
+      }
+      continue;
+    }
+    const int last_key = it.W - 1;
+    const int limit = p.causal ? min(it.shift + i, last_key) : last_key;
+    const int tile_limit = p.causal ? min(it.shift + it.i0 + q * kBM, last_key) : last_key;
     float m_used = -INFINITY, l = 0.f;
 
     for (int j = 0; j < nkv; ++j) {
@@ -898,12 +940,15 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
     if (!mbar_wait(smem_u32(&s.o_full[q]), of & 1u, abort)) return;
     ++of;
     tc_fence_after();
-    const float inv = out_scale / l;
+    // A row that saw no key (chunked calls only) has l = 0 and O = 0.
+    const float inv = l > 0.f ? out_scale / l : 0.f;
     const uint64_t inv2 = f2_pack(inv, inv);
     const bool store = i < it.n;
-    uint4* dst = reinterpret_cast<uint4*>(
-        p.out + static_cast<long long>(it.q_row0 + q * kBM + r) * p.out_tok +
-        static_cast<long long>(it.h) * p.out_head);
+    const long long row = it.q_row0 + q * kBM + r;
+    uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.out_tok + static_cast<long long>(it.h) * p.out_head);
+    if (p.lse && store)
+      p.lse[row * p.lse_tok + static_cast<long long>(it.h) * p.lse_head] =
+          l > 0.f ? (m_used + __log2f(l)) * 0.6931471805599453f : -INFINITY;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
@@ -1000,23 +1045,6 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
     atomicOr(&reinterpret_cast<WsHeader*>(p.ws)->status, MLA_DEVICE_STATUS_TIMEOUT);
 }
 
-// ------------------------------------------------------------ host side
-bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
-
-mla_status_t check_tensor(const mla_tensor_t* t, const char* name, int ndim, mla_dtype_t dtype) {
-  if (!t) return fail(MLA_ERR_INVALID_ARG, "%s descriptor is NULL", name);
-  if (!t->data) return fail(MLA_ERR_INVALID_ARG, "%s data is NULL", name);
-  if (t->ndim != ndim) return fail(MLA_ERR_INVALID_ARG, "%s has ndim %d, expected %d", name, t->ndim, ndim);
-  if (t->dtype != dtype) return fail(MLA_ERR_INVALID_ARG, "%s has dtype %d, expected %d", name, (int)t->dtype, (int)dtype);
-  for (int i = 0; i < ndim; ++i) {
-    if (t->shape[i] < 0 || t->shape[i] > 0x7FFFFFFFll)
-      return fail(MLA_ERR_INVALID_ARG, "%s shape[%d] = %lld out of range", name, i, (long long)t->shape[i]);
-    if (t->stride[i] < 0) return fail(MLA_ERR_INVALID_ARG, "%s stride[%d] is negative", name, i);
-  }
-  if (t->stride[ndim - 1] != 1) return fail(MLA_ERR_INVALID_ARG, "%s innermost stride must be 1", name);
-  return MLA_OK;
-}
-
 }  // namespace
 }  // namespace mla
 
@@ -1036,7 +1064,8 @@ namespace {
 // Launches the scheduler and the attention kernel for one input type.
 template <bool FP8>
 mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t* row_offsets,
-                              const uint32_t* cache_lens, uint32_t B, uint32_t H, uint32_t Tq,
+                              const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
+                              const uint32_t* cache_offsets, uint32_t B, uint32_t H, uint32_t Tq,
                               uint32_t Sk, uint32_t P, uint32_t max_pages, void* workspace,
                               cudaStream_t cs) {
   mla_status_t st;
@@ -1062,9 +1091,9 @@ mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t*
   if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), attn_smem, dev, FP8 ? 3 : 2)) != MLA_OK)
     return st;
   const uint32_t elt = FP8 ? 1u : 2u;
-  schedule_kernel<<<1, kSchedThreads, sched_smem, cs>>>(row_offsets, cache_lens, B, H, Tq, Sk, P,
-                                                        max_pages, elt * (128 + 128),
-                                                        static_cast<uint8_t*>(workspace));
+  schedule_kernel<<<1, kSchedThreads, sched_smem, cs>>>(row_offsets, cache_lens, buffer_row_offsets,
+                                                        cache_offsets, B, H, Tq, Sk, P, max_pages,
+                                                        elt * (128 + 128), static_cast<uint8_t*>(workspace));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "scheduler launch: %s", cudaGetErrorString(e));
   kernel<<<sms, kThreads, attn_smem, cs>>>(prm);
@@ -1073,18 +1102,16 @@ mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t*
   return MLA_OK;
 }
 
-}  // namespace
-}  // namespace mla
-
-extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_tensor_t* q,
-                                           const mla_tensor_t* k_nope, const mla_tensor_t* v,
-                                           const mla_tensor_t* k_rope_pages,
-                                           const mla_tensor_t* page_table,
-                                           const uint32_t* row_offsets, const uint32_t* cache_lens,
-                                           float scale, mla_mask_t mask, void* workspace,
-                                           size_t workspace_bytes, mla_stream_t stream) {
-  using namespace mla;
+// Full-context call (buffer_row_offsets == NULL) or one buffer row of a
+// chunked call (with lse).
+mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla_tensor_t* q,
+                     const mla_tensor_t* k_nope, const mla_tensor_t* v, const mla_tensor_t* k_rope_pages,
+                     const mla_tensor_t* page_table, const uint32_t* row_offsets,
+                     const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
+                     const uint32_t* cache_offsets, float scale, mla_mask_t mask, void* workspace,
+                     size_t workspace_bytes, mla_stream_t stream) {
   mla_status_t st;
+  const bool chunk = buffer_row_offsets != nullptr;
   if (!q) return fail(MLA_ERR_INVALID_ARG, "q descriptor is NULL");
   const bool fp8 = q->dtype == MLA_DTYPE_FP8_E4M3;
   const mla_dtype_t dt = fp8 ? MLA_DTYPE_FP8_E4M3 : MLA_DTYPE_BF16;
@@ -1120,7 +1147,15 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
   if (B < 1 || B > kMaxBatch) return fail(MLA_ERR_INVALID_ARG, "batch %lld outside 1..%u", (long long)B, kMaxBatch);
   if (P < 1 || NP < 1 || max_pages < 1) return fail(MLA_ERR_INVALID_ARG, "empty page pool or page table");
   if (NP * P > 0x7FFFFFFFll) return fail(MLA_ERR_INVALID_ARG, "page pool exceeds 2^31 slots");
-  if (Sk < Tq) return fail(MLA_ERR_INVALID_ARG, "k_nope has fewer rows than q");
+  if (chunk) {
+    if (!cache_offsets) return fail(MLA_ERR_INVALID_ARG, "cache_offsets is NULL");
+    if ((st = check_tensor(lse, "lse", 2, MLA_DTYPE_F32)) != MLA_OK) return st;
+    if (lse->shape[0] != Tq || lse->shape[1] != H) return fail(MLA_ERR_INVALID_ARG, "lse must be [Tq, H] matching q");
+    if (reinterpret_cast<uintptr_t>(lse->data) & 3u) return fail(MLA_ERR_INVALID_ARG, "lse data must be 4-byte aligned");
+    if (Sk < 1) return fail(MLA_ERR_INVALID_ARG, "the buffer row holds no keys");
+  } else if (Sk < Tq) {
+    return fail(MLA_ERR_INVALID_ARG, "k_nope has fewer rows than q");
+  }
   if ((Tq / kQRows + B + 1) * H > 0x7FFFFFFFll)
     return fail(MLA_ERR_INVALID_ARG, "too many work items (query blocks x heads exceeds 2^31)");
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -1203,6 +1238,11 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
   prm.out = static_cast<uint16_t*>(out->data);
   prm.out_tok = out->stride[0];
   prm.out_head = out->stride[1];
+  if (chunk) {
+    prm.lse = static_cast<float*>(lse->data);
+    prm.lse_tok = lse->stride[0];
+    prm.lse_head = lse->stride[1];
+  }
   prm.page_table = static_cast<const uint32_t*>(page_table->data);
   prm.pt_stride = page_table->stride[0];
   prm.rope_base = static_cast<const uint8_t*>(rope_rows);
@@ -1235,9 +1275,35 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
     if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "rope conversion launch: %s", cudaGetErrorString(e));
   }
   auto launch = fp8 ? launch_attention<true> : launch_attention<false>;
-  return launch(prm, dev, sms, row_offsets, cache_lens, static_cast<uint32_t>(B), static_cast<uint32_t>(H),
-                static_cast<uint32_t>(Tq), static_cast<uint32_t>(Sk), static_cast<uint32_t>(P),
-                static_cast<uint32_t>(max_pages), workspace, cs);
+  return launch(prm, dev, sms, row_offsets, cache_lens, buffer_row_offsets, cache_offsets,
+                static_cast<uint32_t>(B), static_cast<uint32_t>(H), static_cast<uint32_t>(Tq),
+                static_cast<uint32_t>(Sk), static_cast<uint32_t>(P), static_cast<uint32_t>(max_pages),
+                workspace, cs);
+}
+
+}  // namespace
+}  // namespace mla
+
+extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_tensor_t* q,
+                                           const mla_tensor_t* k_nope, const mla_tensor_t* v,
+                                           const mla_tensor_t* k_rope_pages,
+                                           const mla_tensor_t* page_table,
+                                           const uint32_t* row_offsets, const uint32_t* cache_lens,
+                                           float scale, mla_mask_t mask, void* workspace,
+                                           size_t workspace_bytes, mla_stream_t stream) {
+  return mla::prefill(out, nullptr, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,
+                      nullptr, nullptr, scale, mask, workspace, workspace_bytes, stream);
+}
+
+extern "C" mla_status_t mla_prefill_ragged_chunk(
+    const mla_tensor_t* out, const mla_tensor_t* lse, const mla_tensor_t* q, const mla_tensor_t* k_nope,
+    const mla_tensor_t* v, const mla_tensor_t* k_rope_pages, const mla_tensor_t* page_table,
+    const uint32_t* row_offsets, const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
+    const uint32_t* cache_offsets, float scale, mla_mask_t mask, void* workspace, size_t workspace_bytes,
+    mla_stream_t stream) {
+  if (!buffer_row_offsets) return mla::fail(MLA_ERR_INVALID_ARG, "buffer_row_offsets is NULL");
+  return mla::prefill(out, lse, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,
+                      buffer_row_offsets, cache_offsets, scale, mask, workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------ no-allocation entry point

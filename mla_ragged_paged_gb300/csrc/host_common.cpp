@@ -87,6 +87,23 @@ mla_status_t set_max_dynamic_smem(const void* func, int bytes, int device, int s
   return MLA_OK;
 }
 
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+mla_status_t check_tensor(const mla_tensor_t* t, const char* name, int ndim, mla_dtype_t dtype) {
+  if (!t) return fail(MLA_ERR_INVALID_ARG, "%s descriptor is NULL", name);
+  if (!t->data) return fail(MLA_ERR_INVALID_ARG, "%s data is NULL", name);
+  if (t->ndim != ndim) return fail(MLA_ERR_INVALID_ARG, "%s has ndim %d, expected %d", name, t->ndim, ndim);
+  if (t->dtype != dtype)
+    return fail(MLA_ERR_INVALID_ARG, "%s has dtype %d, expected %d", name, (int)t->dtype, (int)dtype);
+  for (int i = 0; i < ndim; ++i) {
+    if (t->shape[i] < 0 || t->shape[i] > 0x7FFFFFFFll)
+      return fail(MLA_ERR_INVALID_ARG, "%s shape[%d] = %lld out of range", name, i, (long long)t->shape[i]);
+    if (t->stride[i] < 0) return fail(MLA_ERR_INVALID_ARG, "%s stride[%d] is negative", name, i);
+  }
+  if (t->stride[ndim - 1] != 1) return fail(MLA_ERR_INVALID_ARG, "%s innermost stride must be 1", name);
+  return MLA_OK;
+}
+
 }  // namespace mla
 
 extern "C" const char* mla_last_error_string(void) { return mla::g_error; }

@@ -25,6 +25,12 @@ mla_status_t encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t 
                           const uint64_t* dims, const uint64_t* strides_bytes,
                           const uint32_t* box, CUtensorMapSwizzle swizzle, const char* what);
 
+bool aligned16(const void* ptr);
+
+// Descriptor checks: non-NULL data, rank, dtype, shapes in [0, 2^31),
+// non-negative strides, innermost stride 1.
+mla_status_t check_tensor(const mla_tensor_t* t, const char* name, int ndim, mla_dtype_t dtype);
+
 // Allow `bytes` of dynamic shared memory for `func` on `device` (cached).
 mla_status_t set_max_dynamic_smem(const void* func, int bytes, int device, int slot);
 

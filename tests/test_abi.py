@@ -128,3 +128,66 @@ def test_plan_rejects_bad_arguments(lib):
     assert f(P, P, 2, 32, 4, None, P, P, None, None) == binding.MLA_ERR_INVALID_ARG
     assert f(P, P, 1 << 20, 32, 4, P, P, P, None, None) == binding.MLA_ERR_INVALID_ARG
     assert b"buffer_token_size" in lib.mla_last_error_string() or lib.mla_last_error_string()
+
+
+def _call_chunk(lib, a, lse, bro=0x60000, co=0x70000):
+    r = lambda d: None if d is None else ctypes.byref(d)
+    return lib.mla_prefill_ragged_chunk(r(a["out"]), r(lse), r(a["q"]), r(a["k"]), r(a["v"]),
+                                        r(a["rope"]), r(a["pt"]), a["ro"], a["cl"], bro, co,
+                                        a["scale"], a["mask"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("case", ["no_lse", "lse_shape", "lse_dtype", "lse_unaligned", "no_bro",
+                                  "no_co", "empty_row", "q_depth"])
+def test_chunk_rejects_bad_arguments(lib, case):
+    a = _ragged_args()
+    lse = _desc([10, 2], binding.MLA_DTYPE_F32, ptr=0x80000)
+    bro, co = 0x60000, 0x70000
+    if case == "no_lse":
+        lse = None
+    elif case == "lse_shape":
+        lse = _desc([10, 3], binding.MLA_DTYPE_F32)
+    elif case == "lse_dtype":
+        lse = _desc([10, 2], binding.MLA_DTYPE_BF16)
+    elif case == "lse_unaligned":
+        lse = _desc([10, 2], binding.MLA_DTYPE_F32, ptr=0x80002)
+    elif case == "no_bro":
+        bro = None
+    elif case == "no_co":
+        co = None
+    elif case == "empty_row":
+        a = _ragged_args(k=_desc([0, 2, 128]), v=_desc([0, 2, 128]))
+    elif case == "q_depth":
+        a = _ragged_args(q=_desc([10, 2, 128]))
+    assert _call_chunk(lib, a, lse, bro, co) == binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_last_error_string()
+
+
+@pytest.mark.parametrize("case", ["out_depth", "po_rows", "po_shape", "lse_shape", "lse_dtype",
+                                  "no_ro", "no_bro", "batch0", "po_unaligned"])
+def test_merge_rejects_bad_arguments(lib, case):
+    out = _desc([10, 2, 128])
+    po = _desc([3, 10, 2, 128], ptr=0x90000)
+    pl = _desc([3, 10, 2], binding.MLA_DTYPE_F32, ptr=0xA0000)
+    ro, bro, batch = 0x20000, 0x60000, 2
+    if case == "out_depth":
+        out = _desc([10, 2, 64])
+    elif case == "po_rows":
+        po, pl = _desc([0, 10, 2, 128]), _desc([0, 10, 2], binding.MLA_DTYPE_F32)
+    elif case == "po_shape":
+        po = _desc([3, 10, 3, 128])
+    elif case == "lse_shape":
+        pl = _desc([2, 10, 2], binding.MLA_DTYPE_F32)
+    elif case == "lse_dtype":
+        pl = _desc([3, 10, 2])
+    elif case == "no_ro":
+        ro = None
+    elif case == "no_bro":
+        bro = None
+    elif case == "batch0":
+        batch = 0
+    elif case == "po_unaligned":
+        po = _desc([3, 10, 2, 128], ptr=0x90008)
+    r = lambda d: None if d is None else ctypes.byref(d)
+    assert lib.mla_prefill_merge(r(out), r(po), r(pl), ro, bro, batch, None) == binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_last_error_string()
