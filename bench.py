@@ -12,6 +12,14 @@ the device time of the timed steps.  Under torchrun every rank runs its own
 batch (weak scaling, no data-path collective); the step time is the maximum
 over ranks.
 
+--mode chunked times chunked execution instead of the full-context call: the
+plan, one mla_prefill_ragged_chunk per buffer row of buffer_token_size tokens
+(the K buffer of row r being rows r*T .. r*T+T-1 of the batch-order packed
+K/V), then mla_prefill_merge.  Same metric, same work.
+
+--mode contiguous times mla_prefill_ragged_contiguous: the same K_rope rows laid
+out contiguously (row = K row) instead of paged.
+
 --impl reference times the CPU oracle instead (float64, the machine's host
 cores) on a bounded sample of the same workload.
 """
@@ -219,6 +227,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=[c.name for c in workloads.CONFIGS],
                     help="workload to time (default: the DeepSeek-V3-shaped bf16 batch)")
+    ap.add_argument("--mode", default="full", choices=["full", "chunked", "contiguous"],
+                    help="full-context attention call (paged K_rope), one call per plan buffer row "
+                         "plus the merge, or the full-context call on a contiguous K_rope")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -239,24 +250,56 @@ def main():
     w = workloads.generate(spec if rank == 0 else replace(spec, seed=spec.seed + 1000 * rank))
     F = causal_flops(w)
     d = workloads.device_inputs(w, device=dev)
+    contiguous = args.mode == "contiguous"
+    if contiguous:
+        rows, rsc = workloads.contiguous_rope(w)
+        d["k_rope_contig"] = rows[:, spec.rope_col:spec.rope_col + 64].contiguous().to(dev)
+        del d["k_rope_pool"], d["page_table"]
+        if fp8:
+            d["k_rope_scales"] = rsc.to(dev)
     in_bytes = sum(t.numel() * t.element_size() for t in d.values())
     Tq, H, B = w.total_q, w.heads, w.batch
     T = spec.buffer_token_size
     R = (w.total_k + T - 1) // T
     out = torch.empty((Tq, H, 128), dtype=torch.bfloat16, device=dev)
-    ws = binding.alloc_workspace(B, dev, fp8_pool_slots=w.num_pages * w.page_size if fp8 else None)
+    ws = binding.alloc_workspace(B, dev, fp8_pool_slots=(w.total_k if contiguous else w.num_pages * w.page_size)
+                                 if fp8 else None)
     scales = {k: d.get(k) for k in ("q_scale", "k_scale", "v_scale", "k_rope_scales")}
     plan_out = (torch.empty((R, B + 1), dtype=torch.int32, device=dev),
                 torch.empty((R, B), dtype=torch.int32, device=dev),
                 torch.empty((R,), dtype=torch.int32, device=dev),
                 torch.empty((1,), dtype=torch.int32, device=dev))
     stream = torch.cuda.current_stream(dev)
+    chunked = args.mode == "chunked"
+    scratch = binding.chunked_scratch(R, Tq, H, dev) if chunked else None
+
+    def attention(inp, o, mark=None):
+        """The attention part of a step; `mark` (an event) is recorded between
+        the per-row calls and the merge in chunked mode."""
+        if contiguous:
+            binding.prefill_ragged_contiguous(o, inp["q"], inp["k_nope"], inp["v"], inp["k_rope_contig"],
+                                              inp["row_offsets"], inp["cache_lens"], w.scale,
+                                              binding.MLA_MASK_CAUSAL, ws, stream=stream, **scales)
+            return
+        if not chunked:
+            binding.prefill_ragged(o, inp["q"], inp["k_nope"], inp["v"], inp["k_rope_pool"],
+                                   inp["page_table"], inp["row_offsets"], inp["cache_lens"], w.scale,
+                                   binding.MLA_MASK_CAUSAL, ws, stream=stream, **scales)
+            return
+        po, pl = scratch
+        for r in range(R):
+            lo, hi = r * T, min((r + 1) * T, w.total_k)
+            binding.prefill_ragged_chunk(po[r], pl[r], inp["q"], inp["k_nope"][lo:hi], inp["v"][lo:hi],
+                                         inp["k_rope_pool"], inp["page_table"], inp["row_offsets"],
+                                         inp["cache_lens"], plan_out[0][r], plan_out[1][r], w.scale,
+                                         binding.MLA_MASK_CAUSAL, ws, stream=stream, **scales)
+        if mark is not None:
+            mark.record(stream)
+        binding.merge(o, po, pl, inp["row_offsets"], plan_out[0], stream=stream)
 
     def step(inp, o):
         binding.plan(inp["row_offsets"], inp["cache_lens"], T, R, stream=stream, out=plan_out)
-        binding.prefill_ragged(o, inp["q"], inp["k_nope"], inp["v"], inp["k_rope_pool"],
-                               inp["page_table"], inp["row_offsets"], inp["cache_lens"], w.scale,
-                               binding.MLA_MASK_CAUSAL, ws, stream=stream, **scales)
+        attention(inp, o)
 
     for _ in range(args.warmup):
         step(d, out)
@@ -264,8 +307,7 @@ def main():
 
     # Device-resident timing: per-step events around the attention call and
     # around the whole step, on the launching stream.
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
     barrier(world)
     with ClockSampler(local) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
@@ -275,21 +317,26 @@ def main():
             ev[i][0].record(stream)
             binding.plan(d["row_offsets"], d["cache_lens"], T, R, stream=stream, out=plan_out)
             ev[i][1].record(stream)
-            binding.prefill_ragged(out, d["q"], d["k_nope"], d["v"], d["k_rope_pool"],
-                                   d["page_table"], d["row_offsets"], d["cache_lens"], w.scale,
-                                   binding.MLA_MASK_CAUSAL, ws, stream=stream, **scales)
-            ev[i][2].record(stream)
+            attention(d, out, mark=ev[i][2] if chunked else None)
+            ev[i][3].record(stream)
         t_end.record(stream)
         barrier(world)
     total_ms = dist_max(t_start.elapsed_time(t_end), world)
-    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    # Attention-kernel span (the per-row calls in chunked mode) and merge span.
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2] if chunked else e[3]) for e in ev)
+    merge_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) if chunked else None
     assert binding.device_status(ws) == 0, "device status after timed steps"
     clocks = clk.summary()
 
     # End to end through the public API: pinned host inputs -> device, plan +
     # attention, output -> pinned host, every step.
     h = workloads.device_inputs(w, device="cpu", pin=True)
-    keys = ["q", "k_nope", "v", "k_rope_pool", "page_table", "row_offsets", "cache_lens"]
+    if contiguous:
+        h["k_rope_contig"] = d["k_rope_contig"].cpu().pin_memory()
+        if fp8:
+            h["k_rope_scales"] = d["k_rope_scales"].cpu().pin_memory()
+    keys = ["q", "k_nope", "v", "row_offsets", "cache_lens"]
+    keys += ["k_rope_contig"] if contiguous else ["k_rope_pool", "page_table"]
     if fp8:
         keys += ["q_scale", "k_scale", "v_scale", "k_rope_scales"]
     d2 = {k: torch.empty_like(d[k]) for k in keys}
@@ -322,8 +369,19 @@ def main():
     peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
     achieved = F / (attn_ms * 1e-3) / 1e12
     traffic = None
-    if ATTENTION_TRAFFIC["source_sha1"] == source_sha1():
+    if ATTENTION_TRAFFIC["source_sha1"] == source_sha1() and args.mode == "full":
         traffic = ATTENTION_TRAFFIC["bytes_per_launch"].get(spec.name)
+    merge_roofline = None
+    if chunked:
+        # Algorithmic merge bytes: per (token, head), 256 + 4 bytes read from
+        # each row holding keys of its sequence, 256 bytes written.
+        G = np.concatenate([[0], np.cumsum(w.n + w.prior)])
+        rows_b = (np.minimum(-(-G[1:] // T), R) - G[:-1] // T) * ((w.n + w.prior) > 0)
+        mbytes = H * int(sum(int(w.n[b]) * (int(rows_b[b]) * 260 + 256) for b in range(B)))
+        m_gbs = mbytes / (merge_ms * 1e-3) / 1e9
+        merge_roofline = {"bound": "hbm", "achieved": m_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": m_gbs / peaks["hbm_gbs"], "bytes_per_launch": mbytes,
+                          "ms": merge_ms, "kernel": "merge_kernel"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -343,18 +401,24 @@ def main():
                        "total_q_tokens": Tq, "heads": H, "causal_effective_tflop_per_step": F / 1e12,
                        "parallelism": f"dp{world} (independent batches)" if world > 1 else "none",
                        "l2": f"inputs ({in_bytes / 1e9:.2f} GB) larger than L2; no flush",
-                       "step": "mla_prefill_plan + mla_prefill_ragged"},
+                       "step": ("mla_prefill_plan + %d x mla_prefill_ragged_chunk (T=%d) + mla_prefill_merge"
+                                % (R, T)) if chunked else
+                               ("mla_prefill_plan + mla_prefill_ragged_contiguous (K_rope [S_k, 64], not paged)"
+                                if contiguous else "mla_prefill_plan + mla_prefill_ragged")},
             "pct_of_peak": 100.0 * value / world / peak,
             "clocks": clocks,
             "e2e": {"value": world * F * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": (4 if fp8 else 3) * args.steps,
+            "gpu_launches": ((2 + R * (3 if fp8 else 2)) if chunked else (4 if fp8 else 3)) * args.steps,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "mla_attention_kernel (+ its 1-CTA scheduler launch in the span)",
+                         "kernel": ("mla_attention_kernel over %d buffer rows (+ their scheduler launches)" % R)
+                                   if chunked else "mla_attention_kernel (+ its 1-CTA scheduler launch in the span)",
                          "peak_source": f"{peak_src} bf16_tflops (burst)" + (" x 2 (fp8/bf16 nominal ratio)" if fp8 else "")},
             "cpu_baseline": cpu,
         }
+        if chunked:
+            line["roofline_merge"] = merge_roofline
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -173,6 +173,32 @@ mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_tensor_t* q,
                                 size_t workspace_bytes, mla_stream_t stream);
 
 /*
+ * Ragged MLA prefill attention with a contiguous K_rope (flare_mla_prefill:
+ * the overload taking k_rope as a plain tensor, and cache_offsets, which is
+ * None "when the cache is contiguous").
+ *
+ * As mla_prefill_ragged, except that K_rope is not paged: k_rope row
+ * G_b + j holds the 64 rope dims of key j of sequence b, the same row as
+ * k_nope / v, so K[j] = [ k_nope[G_b + j, h, :] , k_rope[G_b + j, :] ].
+ *   k_rope       device [Sk, 64] (rows = k_nope's rows), bf16 with bf16 q;
+ *                fp8 with fp8 q, with one float scale per row
+ *                (scale_gran MLA_SCALE_PER_TOKEN, index = row).  The row
+ *                stride may exceed 64 (the rope tail of a wider latent row)
+ *                and must be a multiple of 16 bytes.
+ *   batch        B >= 1 (no page table carries it); row_offsets has B+1
+ *                entries, cache_lens B.
+ *   workspace    >= mla_prefill_ragged_workspace_size(B) for bf16 inputs,
+ *                >= mla_prefill_ragged_workspace_size_fp8(B, Sk) for fp8.
+ * Each 128-key tile's K_rope arrives as one TMA box (no page lookups).
+ */
+mla_status_t mla_prefill_ragged_contiguous(const mla_tensor_t* out, const mla_tensor_t* q,
+                                           const mla_tensor_t* k_nope, const mla_tensor_t* v,
+                                           const mla_tensor_t* k_rope, const uint32_t* row_offsets,
+                                           const uint32_t* cache_lens, uint32_t batch, float scale,
+                                           mla_mask_t mask, void* workspace, size_t workspace_bytes,
+                                           mla_stream_t stream);
+
+/*
  * mla_prefill_ragged for callers that cannot allocate device memory.  No
  * counterpart on the reference pages: it exists for callers such as a plug-in
  * whose host framework owns all device memory and offers it no scratch

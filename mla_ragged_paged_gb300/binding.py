@@ -21,7 +21,8 @@ STATUS_BITS = {0x1: "BAD_PAGE", 0x2: "BAD_COLUMN", 0x4: "BAD_OFFSETS", 0x8: "TIM
 # Names exported by the C ABI (kept in step with include/mla_prefill.h).
 EXPORTS = ["mla_prefill_plan", "mla_prefill_plan_max_rows", "mla_prefill_ragged_workspace_size",
            "mla_prefill_ragged_workspace_size_fp8", "mla_prefill_ragged", "mla_prefill_ragged_noalloc",
-           "mla_prefill_ragged_chunk", "mla_prefill_merge", "mla_read_device_status",
+           "mla_prefill_ragged_chunk", "mla_prefill_merge", "mla_prefill_ragged_contiguous",
+           "mla_read_device_status",
            "mla_last_error_string"]
 
 
@@ -69,6 +70,9 @@ def load(path=LIB_PATH):
     lib.mla_prefill_ragged_chunk.restype = ctypes.c_int
     lib.mla_prefill_merge.argtypes = [pt, pt, pt, vp, vp, u32, vp]
     lib.mla_prefill_merge.restype = ctypes.c_int
+    lib.mla_prefill_ragged_contiguous.argtypes = [pt, pt, pt, pt, pt, vp, vp, u32, ctypes.c_float,
+                                                  ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.mla_prefill_ragged_contiguous.restype = ctypes.c_int
     lib.mla_read_device_status.argtypes = [vp, ctypes.POINTER(u32), vp]
     lib.mla_read_device_status.restype = ctypes.c_int
     lib.mla_last_error_string.argtypes = []
@@ -215,6 +219,30 @@ def prefill_ragged_chunk(out, lse, q, k_nope, v, k_rope_pages, page_table, row_o
                                         int(mask), _ptr(workspace), workspace.numel(),
                                         _stream(stream)))
     return out, lse
+
+
+def prefill_ragged_contiguous(out, q, k_nope, v, k_rope, row_offsets, cache_lens, scale,
+                              mask=MLA_MASK_CAUSAL, workspace=None, q_scale=None, k_scale=None,
+                              v_scale=None, k_rope_scales=None, stream=None):
+    """mla_prefill_ragged_contiguous: k_rope is [Sk, 64], row r the rope part of
+    k_nope row r; fp8 inputs take one K_rope scale per row ([Sk] float32)."""
+    lib = load()
+    B = row_offsets.numel() - 1
+    fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
+    if workspace is None:
+        workspace = alloc_workspace(B, q.device, k_rope.shape[0] if fp8 else None)
+    gran_t = MLA_SCALE_PER_TENSOR if fp8 else MLA_SCALE_NONE
+    d_out = describe(out, MLA_DTYPE_BF16)
+    d_q = describe(q, _dtype_code(q), q_scale if fp8 else None, gran_t)
+    d_k = describe(k_nope, _dtype_code(k_nope), k_scale if fp8 else None, gran_t)
+    d_v = describe(v, _dtype_code(v), v_scale if fp8 else None, gran_t)
+    d_r = describe(k_rope, _dtype_code(k_rope), k_rope_scales if fp8 else None,
+                   MLA_SCALE_PER_TOKEN if fp8 else MLA_SCALE_NONE)
+    _check(lib.mla_prefill_ragged_contiguous(ctypes.byref(d_out), ctypes.byref(d_q), ctypes.byref(d_k),
+                                             ctypes.byref(d_v), ctypes.byref(d_r), _ptr(row_offsets),
+                                             _ptr(cache_lens), B, float(scale), int(mask),
+                                             _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
 
 
 def merge(out, partial_out, partial_lse, row_offsets, buffer_row_offsets, stream=None):

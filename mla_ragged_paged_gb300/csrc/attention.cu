@@ -113,6 +113,7 @@ struct AttnParams {
   const uint8_t* rope_base;
   long long rope_tok_bytes, rope_page_bytes;
   uint32_t max_pages, num_pages, page_size, rope_box, rope_manual;
+  uint32_t rope_contig;  // K_rope row = K row (no page table)
   uint32_t H, causal;
   float sl2;
   uint8_t* ws;
@@ -406,6 +407,12 @@ __device__ __forceinline__ bool read_item(Smem<FP8>& s, uint32_t& item_k, int la
 // per group.  A slot's full barrier therefore completes a phase only when the
 // slot heads a group; both sides keep one phase bit per slot.  Empty barriers
 // stay per chunk (one UMMA commit each).
+// One lane's page-table read for a K_rope box: state 0 = no box, 1 = page
+// read, 2 = page-table column out of range.
+struct RopeFetch {
+  uint32_t page, row, state;
+};
+
 template <bool FP8>
 __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volatile uint32_t* abort) {
   using C = Cfg<FP8>;
@@ -433,26 +440,28 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
   };
   // bf16 K_rope rows into slot `ps`: TMA boxes (one per page segment, lane t
   // owns box t) when page segments are 8-row aligned, else a swizzled row
-  // gather.  Window key `key` is context position co + key.
-  auto rope_lookup = [&](const ItemInfo& it, int j, uint32_t& page, uint32_t& row_in_page) -> bool {
+  // gather.  Window key `key` is context position co + key.  The page-table
+  // reads for a tile's boxes are issued one tile ahead (rope_fetch) and only
+  // checked when the boxes go out, so their latency hides behind the ring
+  // waits in between.
+  auto rope_fetch = [&](const ItemInfo& it, int j) -> RopeFetch {
+    RopeFetch f = {0u, 0u, 0u};
     const int nbox = kBN / static_cast<int>(p.rope_box);
-    bool issue = false;
     if (lane < nbox) {
       const int key = j * kBN + lane * static_cast<int>(p.rope_box);
       if (key < it.W) {
         const uint32_t a = static_cast<uint32_t>(it.co + key);
         const uint32_t col = a / p.page_size;
-        row_in_page = a - col * p.page_size;
+        f.row = a - col * p.page_size;
         if (col >= p.max_pages) {
-          status |= MLA_DEVICE_STATUS_BAD_COLUMN;
+          f.state = 2;
         } else {
-          page = p.page_table[static_cast<long long>(it.b) * p.pt_stride + col];
-          if (page >= p.num_pages) status |= MLA_DEVICE_STATUS_BAD_PAGE;
-          else issue = true;
+          f.page = p.page_table[static_cast<long long>(it.b) * p.pt_stride + col];
+          f.state = 1;
         }
       }
     }
-    return issue;
+    return f;
   };
   auto rope_gather = [&](const ItemInfo& it, int j, uint32_t ps) {
     const uint32_t dst = ring.buf(ps);
@@ -482,16 +491,25 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
   // The K group of tile j: K_nope chunks (bf16: [0:64] and [64:128] at k,
   // k+1; fp8: one 128-code chunk at k), then the bf16 K_rope chunk (for fp8
   // inputs read from the converted copy of the pool).
-  auto load_k_group = [&](const ItemInfo& it, int j, uint32_t k) -> bool {
+  auto load_k_group = [&](const ItemInfo& it, int j, uint32_t k, bool boxes, const RopeFetch& rf) -> bool {
     constexpr int kNope = FP8 ? 1 : 2;
     const uint32_t bar = ring.full_bar(k);
     const uint32_t kr = k + kNope;  // K_rope slot
     for (int c = 0; c <= kNope; ++c)
       if (!acquire(k + c)) return false;
-    // A window that starts inside a page segment takes the row gather.
-    if (!p.rope_manual && it.co % static_cast<int>(p.rope_box) == 0) {
-      uint32_t page = 0, row_in_page = 0;
-      const bool issue = rope_lookup(it, j, page, row_in_page);
+    if (p.rope_contig) {
+      // Contiguous K_rope: the tile's 128 rows sit at its K rows.
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, (kNope + 1) * kChunk);
+        for (int c = 0; c < kNope; ++c) tma_chunk(&p.tm_k, 64 * c, it, j, k + c, bar);
+        tma_load_2d(ring.buf(kr), &p.tm_rope, bar, 0, it.kv_row0 + j * kBN);
+      }
+      __syncwarp();
+    } else if (boxes) {
+      bool issue = false;
+      if (rf.state == 2) status |= MLA_DEVICE_STATUS_BAD_COLUMN;
+      else if (rf.state == 1 && rf.page >= p.num_pages) status |= MLA_DEVICE_STATUS_BAD_PAGE;
+      else issue = rf.state == 1;
       const uint32_t mask = __ballot_sync(0xffffffffu, issue);
       const uint32_t bytes = kNope * kChunk + __popc(mask) * p.rope_box * 128u;
       if (lane == 0) {
@@ -501,7 +519,7 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
       __syncwarp();
       if (issue)
         tma_load_3d(ring.buf(kr) + lane * p.rope_box * 128u, &p.tm_rope, bar, 0,
-                    static_cast<int>(row_in_page), static_cast<int>(page));
+                    static_cast<int>(rf.row), static_cast<int>(rf.page));
     } else {
       rope_gather(it, j, kr);
       if (lane == 0) {
@@ -552,9 +570,16 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     ++item_k;
     if (!it.valid) break;
     const int nkv = it.n1 > 0 ? it.nkv1 : it.nkv0;
+    // K_rope by one TMA box per page segment, unless the rows are contiguous
+    // or the segments are not 8-row aligned (pages, or a window that starts
+    // inside a segment): then the row gather.
+    const bool boxes = !p.rope_contig && !p.rope_manual && it.co % static_cast<int>(p.rope_box) == 0;
+    RopeFetch rf = {0u, 0u, 0u};
+    if (boxes && nkv > 0) rf = rope_fetch(it, 0);
     for (int j = 0; j < nkv && alive; ++j) {
       const TilePos tp = tile_pos<FP8>(pos);
-      alive = load_k_group(it, j, tp.k);
+      alive = load_k_group(it, j, tp.k, boxes, rf);
+      if (boxes && j + 1 < nkv) rf = rope_fetch(it, j + 1);
       // A query tile that sees no key of the window is not loaded.
       if (alive && j == 0) alive = (it.nkv0 == 0 || load_q(0, it)) && (it.nkv1 == 0 || load_q(1, it));
       if (alive && tp.pad != kNoPad) {  // pad slot: keeps the V pair adjacent
@@ -1104,14 +1129,17 @@ mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t*
 
 // Full-context call (buffer_row_offsets == NULL) or one buffer row of a
 // chunked call (with lse).
+// page_table == NULL: K_rope is contiguous, k_rope_pages is [Sk, 64] with row
+// r holding the rope part of k_nope row r, and contig_batch gives B.
 mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla_tensor_t* q,
                      const mla_tensor_t* k_nope, const mla_tensor_t* v, const mla_tensor_t* k_rope_pages,
-                     const mla_tensor_t* page_table, const uint32_t* row_offsets,
+                     const mla_tensor_t* page_table, uint32_t contig_batch, const uint32_t* row_offsets,
                      const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
                      const uint32_t* cache_offsets, float scale, mla_mask_t mask, void* workspace,
                      size_t workspace_bytes, mla_stream_t stream) {
   mla_status_t st;
   const bool chunk = buffer_row_offsets != nullptr;
+  const bool contig = page_table == nullptr;
   if (!q) return fail(MLA_ERR_INVALID_ARG, "q descriptor is NULL");
   const bool fp8 = q->dtype == MLA_DTYPE_FP8_E4M3;
   const mla_dtype_t dt = fp8 ? MLA_DTYPE_FP8_E4M3 : MLA_DTYPE_BF16;
@@ -1119,8 +1147,9 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   if ((st = check_tensor(out, "out", 3, MLA_DTYPE_BF16)) != MLA_OK) return st;
   if ((st = check_tensor(k_nope, "k_nope", 3, dt)) != MLA_OK) return st;
   if ((st = check_tensor(v, "v", 3, dt)) != MLA_OK) return st;
-  if ((st = check_tensor(k_rope_pages, "k_rope_pages", 3, dt)) != MLA_OK) return st;
-  if ((st = check_tensor(page_table, "page_table", 2, MLA_DTYPE_U32)) != MLA_OK) return st;
+  if ((st = check_tensor(k_rope_pages, contig ? "k_rope" : "k_rope_pages", contig ? 2 : 3, dt)) != MLA_OK)
+    return st;
+  if (!contig && (st = check_tensor(page_table, "page_table", 2, MLA_DTYPE_U32)) != MLA_OK) return st;
   if (fp8) {
     const mla_tensor_t* pt[3] = {q, k_nope, v};
     const char* pn[3] = {"q", "k_nope", "v"};
@@ -1135,14 +1164,21 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   if (!(scale >= 0.f) || !std::isfinite(scale)) return fail(MLA_ERR_INVALID_ARG, "scale must be finite and >= 0");
 
   const int64_t Tq = q->shape[0], H = q->shape[1], Sk = k_nope->shape[0];
-  const int64_t B = page_table->shape[0], max_pages = page_table->shape[1];
-  const int64_t NP = k_rope_pages->shape[0], P = k_rope_pages->shape[1];
+  // A contiguous K_rope is addressed like a pool of one-row pages whose page
+  // id is the K row; the page table is not read.
+  const int64_t B = contig ? static_cast<int64_t>(contig_batch) : page_table->shape[0];
+  const int64_t max_pages = contig ? 0xFFFFFFFFll : page_table->shape[1];
+  const int64_t NP = k_rope_pages->shape[0], P = contig ? 1 : k_rope_pages->shape[1];
   if (q->shape[2] != 192) return fail(MLA_ERR_INVALID_ARG, "q depth must be 192");
   if (out->shape[0] != Tq || out->shape[1] != H || out->shape[2] != 128)
     return fail(MLA_ERR_INVALID_ARG, "out must be [Tq, H, 128] matching q");
   if (k_nope->shape[1] != H || k_nope->shape[2] != 128) return fail(MLA_ERR_INVALID_ARG, "k_nope must be [Sk, H, 128]");
   if (v->shape[0] != Sk || v->shape[1] != H || v->shape[2] != 128) return fail(MLA_ERR_INVALID_ARG, "v must be [Sk, H, 128] matching k_nope");
-  if (k_rope_pages->shape[2] != 64) return fail(MLA_ERR_INVALID_ARG, "k_rope_pages must be [num_pages, P, 64]");
+  if (contig) {
+    if (NP != Sk || k_rope_pages->shape[1] != 64) return fail(MLA_ERR_INVALID_ARG, "k_rope must be [Sk, 64] matching k_nope");
+  } else if (k_rope_pages->shape[2] != 64) {
+    return fail(MLA_ERR_INVALID_ARG, "k_rope_pages must be [num_pages, P, 64]");
+  }
   if (H < 1) return fail(MLA_ERR_INVALID_ARG, "num_heads must be >= 1");
   if (B < 1 || B > kMaxBatch) return fail(MLA_ERR_INVALID_ARG, "batch %lld outside 1..%u", (long long)B, kMaxBatch);
   if (P < 1 || NP < 1 || max_pages < 1) return fail(MLA_ERR_INVALID_ARG, "empty page pool or page table");
@@ -1171,7 +1207,7 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   for (int i = 0; i < 5; ++i) {
     const int64_t es = (i < 4 && fp8) ? 1 : 2;
     if (!aligned16(ts[i]->data)) return fail(MLA_ERR_INVALID_ARG, "%s data must be 16-byte aligned", names[i]);
-    for (int d = 0; d < 2; ++d)
+    for (int d = 0; d < ts[i]->ndim - 1; ++d)
       if ((ts[i]->stride[d] * es) % 16 != 0 || ts[i]->stride[d] * es >= (1ll << 40))
         return fail(MLA_ERR_INVALID_ARG, "%s stride[%d] must be a multiple of 16 bytes", names[i], d);
   }
@@ -1215,19 +1251,29 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     while (b) { uint32_t t = a % b; a = b; b = t; }
     g = a;  // gcd(P, 128): rows per page segment inside a key tile
   }
-  prm.rope_manual = (g % 8u) != 0;
-  prm.rope_box = g;
+  prm.rope_contig = contig;
+  prm.rope_manual = !contig && (g % 8u) != 0;
+  prm.rope_box = contig ? kBN : g;
   // bf16 K_rope rows: the caller's pool, or for fp8 inputs the converted copy
   // the pre-pass writes after the scheduler records in the workspace.
+  const int64_t rope_tok_el = contig ? k_rope_pages->stride[0] : k_rope_pages->stride[1];
   void* rope_rows = k_rope_pages->data;
-  uint64_t rope_tok = static_cast<uint64_t>(k_rope_pages->stride[1]) * 2;
+  uint64_t rope_tok = static_cast<uint64_t>(rope_tok_el) * 2;
   uint64_t rope_page = static_cast<uint64_t>(k_rope_pages->stride[0]) * 2;
   if (fp8) {
     rope_rows = static_cast<uint8_t*>(workspace) + mla_prefill_ragged_workspace_size(static_cast<uint32_t>(B));
     rope_tok = 128;
     rope_page = static_cast<uint64_t>(P) * 128;
   }
-  if (!prm.rope_manual) {
+  if (contig) {
+    // One 128-row box per KV tile, at the tile's K row.
+    uint64_t dims[2] = {64, (uint64_t)NP};
+    uint64_t str[1] = {rope_tok};
+    uint32_t box[2] = {64, kBN};
+    if ((st = encode_tiled(&prm.tm_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rope_rows, dims, str, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "k_rope")) != MLA_OK)
+      return st;
+  } else if (!prm.rope_manual) {
     uint64_t dims[3] = {64, (uint64_t)P, (uint64_t)NP};
     uint64_t str[2] = {rope_tok, rope_page};
     uint32_t box[3] = {64, g, 1};
@@ -1243,8 +1289,8 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     prm.lse_tok = lse->stride[0];
     prm.lse_head = lse->stride[1];
   }
-  prm.page_table = static_cast<const uint32_t*>(page_table->data);
-  prm.pt_stride = page_table->stride[0];
+  prm.page_table = contig ? nullptr : static_cast<const uint32_t*>(page_table->data);
+  prm.pt_stride = contig ? 0 : page_table->stride[0];
   prm.rope_base = static_cast<const uint8_t*>(rope_rows);
   prm.rope_tok_bytes = static_cast<long long>(rope_tok);
   prm.rope_page_bytes = static_cast<long long>(rope_page);
@@ -1269,7 +1315,7 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     const uint32_t slots = static_cast<uint32_t>(NP * P);
     const int blocks = static_cast<int>(std::min<uint32_t>((slots + 255) / 256, 16u * sms));
     rope_convert_kernel<<<blocks, 256, 0, cs>>>(
-        static_cast<const uint8_t*>(k_rope_pages->data), k_rope_pages->stride[1], k_rope_pages->stride[0],
+        static_cast<const uint8_t*>(k_rope_pages->data), rope_tok_el, k_rope_pages->stride[0],
         static_cast<uint32_t>(P), slots, k_rope_pages->scale, k_nope->scale, static_cast<uint16_t*>(rope_rows));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "rope conversion launch: %s", cudaGetErrorString(e));
@@ -1291,7 +1337,20 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
                                            const uint32_t* row_offsets, const uint32_t* cache_lens,
                                            float scale, mla_mask_t mask, void* workspace,
                                            size_t workspace_bytes, mla_stream_t stream) {
-  return mla::prefill(out, nullptr, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,
+  if (!page_table) return mla::fail(MLA_ERR_INVALID_ARG, "page_table descriptor is NULL");
+  return mla::prefill(out, nullptr, q, k_nope, v, k_rope_pages, page_table, 0, row_offsets, cache_lens,
+                      nullptr, nullptr, scale, mask, workspace, workspace_bytes, stream);
+}
+
+extern "C" mla_status_t mla_prefill_ragged_contiguous(const mla_tensor_t* out, const mla_tensor_t* q,
+                                                      const mla_tensor_t* k_nope, const mla_tensor_t* v,
+                                                      const mla_tensor_t* k_rope,
+                                                      const uint32_t* row_offsets,
+                                                      const uint32_t* cache_lens, uint32_t batch,
+                                                      float scale, mla_mask_t mask, void* workspace,
+                                                      size_t workspace_bytes, mla_stream_t stream) {
+  if (batch < 1) return mla::fail(MLA_ERR_INVALID_ARG, "batch must be >= 1");
+  return mla::prefill(out, nullptr, q, k_nope, v, k_rope, nullptr, batch, row_offsets, cache_lens,
                       nullptr, nullptr, scale, mask, workspace, workspace_bytes, stream);
 }
 
@@ -1302,7 +1361,8 @@ extern "C" mla_status_t mla_prefill_ragged_chunk(
     const uint32_t* cache_offsets, float scale, mla_mask_t mask, void* workspace, size_t workspace_bytes,
     mla_stream_t stream) {
   if (!buffer_row_offsets) return mla::fail(MLA_ERR_INVALID_ARG, "buffer_row_offsets is NULL");
-  return mla::prefill(out, lse, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,
+  if (!page_table) return mla::fail(MLA_ERR_INVALID_ARG, "page_table descriptor is NULL");
+  return mla::prefill(out, lse, q, k_nope, v, k_rope_pages, page_table, 0, row_offsets, cache_lens,
                       buffer_row_offsets, cache_offsets, scale, mask, workspace, workspace_bytes, stream);
 }
 

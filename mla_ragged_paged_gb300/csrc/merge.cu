@@ -17,14 +17,11 @@ namespace mla {
 namespace {
 
 constexpr int kMergeThreads = 256;
+constexpr int kBatch = 4;  // rows whose loads are in flight together
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+__device__ __forceinline__ uint4 ld_nc_v4(const uint16_t* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
 __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
@@ -64,28 +61,48 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     float m = -INFINITY, den = 0.f, acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    for (uint32_t r = 0; r < p.R; ++r) {
-      const uint32_t* row = p.bro + static_cast<size_t>(r) * (p.B + 1);
-      if (row[b + 1] <= row[b]) continue;  // sequence b has no keys in row r
-      const float ls = p.pl[r * p.pl_row + t * p.pl_tok + h * p.pl_head];
-      if (!(ls > -INFINITY) || !(ls < INFINITY)) continue;
-      const uint4 v = ld_nc_v4(p.po + r * p.po_row + t * p.po_tok + h * p.po_head + 8 * c);
-      if (ls > m) {
-        const float cr = ex2_approx((m - ls) * kLog2e);  // 0 while m = -inf
+    // Rows in batches of kBatch: every load of a batch is issued before any
+    // is used, so a thread keeps kBatch 16-byte reads in flight.
+    for (uint32_t r0 = 0; r0 < p.R; r0 += kBatch) {
+      float ls[kBatch];
+      uint4 v[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const uint32_t r = r0 + k;
+        ls[k] = -INFINITY;
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < p.R) {
+          const uint32_t* row = p.bro + static_cast<size_t>(r) * (p.B + 1);
+          if (row[b + 1] > row[b]) {  // sequence b has keys in row r
+            ls[k] = p.pl[r * p.pl_row + t * p.pl_tok + h * p.pl_head];
+            v[k] = ld_nc_v4(p.po + r * p.po_row + t * p.po_tok + h * p.po_head + 8 * c);
+          }
+        }
+      }
+      float mb = m;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (ls[k] > mb && ls[k] < INFINITY) mb = ls[k];
+      if (mb > m) {
+        const float cr = ex2_approx((m - mb) * kLog2e);  // 0 while m = -inf
         den *= cr;
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] *= cr;
-        m = ls;
+        m = mb;
       }
-      const float wgt = ex2_approx((ls - m) * kLog2e);
-      den += wgt;
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float x0, x1;
-        bf16x2_to_f32(w[e], x0, x1);
-        acc[2 * e] = fmaf(wgt, x0, acc[2 * e]);
-        acc[2 * e + 1] = fmaf(wgt, x1, acc[2 * e + 1]);
+      for (int k = 0; k < kBatch; ++k) {
+        if (!(ls[k] > -INFINITY) || !(ls[k] < INFINITY)) continue;
+        const float wgt = ex2_approx((ls[k] - m) * kLog2e);
+        den += wgt;
+        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float x0, x1;
+          bf16x2_to_f32(w[e], x0, x1);
+          acc[2 * e] = fmaf(wgt, x0, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(wgt, x1, acc[2 * e + 1]);
+        }
       }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;

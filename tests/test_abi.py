@@ -191,3 +191,25 @@ def test_merge_rejects_bad_arguments(lib, case):
     r = lambda d: None if d is None else ctypes.byref(d)
     assert lib.mla_prefill_merge(r(out), r(po), r(pl), ro, bro, batch, None) == binding.MLA_ERR_INVALID_ARG
     assert lib.mla_last_error_string()
+
+
+@pytest.mark.parametrize("case", ["rope_3d", "rope_rows", "rope_depth", "batch0", "rope_stride"])
+def test_contiguous_rejects_bad_arguments(lib, case):
+    a = _ragged_args()
+    rope, batch = _desc([20, 64]), 2
+    if case == "rope_3d":
+        rope = _desc([4, 16, 64])
+    elif case == "rope_rows":
+        rope = _desc([19, 64])
+    elif case == "rope_depth":
+        rope = _desc([20, 32])
+    elif case == "batch0":
+        batch = 0
+    elif case == "rope_stride":
+        rope.stride[0] = 68       # 136 bytes
+    r = ctypes.byref
+    st = lib.mla_prefill_ragged_contiguous(r(a["out"]), r(a["q"]), r(a["k"]), r(a["v"]), r(rope),
+                                           a["ro"], a["cl"], batch, a["scale"], a["mask"], a["ws"],
+                                           a["ws_bytes"], None)
+    assert st == binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_last_error_string()

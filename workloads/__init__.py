@@ -310,3 +310,24 @@ def device_inputs(w: Workload, device="cuda", pin=False):
         d["v_scale"] = mv(torch.tensor([w.v_scale], dtype=torch.float32))
         d["k_rope_scales"] = mv(w.k_rope_scales)
     return d
+
+
+def contiguous_rope(w: Workload):
+    """The same K_rope laid out contiguously, as a cache without pages holds it:
+    row G_b + j = the pool row of key j of sequence b (the page table's
+    placement undone).  Returns ([S_k, row_width] tensor of the pool's dtype,
+    [S_k] float32 per-row scales or None for bf16)."""
+    P = w.page_size
+    slots = np.empty(w.total_k, dtype=np.int64)
+    G = 0
+    for b in range(w.batch):
+        L = int(w.n[b] + w.prior[b])
+        j = np.arange(L)
+        slots[G:G + L] = w.page_table[b, j // P].astype(np.int64) * P + j % P
+        G += L
+    idx = torch.from_numpy(slots)
+    rows = w.k_rope_pool.reshape(-1, w.k_rope_pool.shape[-1])[idx].contiguous()
+    scales = None
+    if w.spec.dtype == "fp8":
+        scales = w.k_rope_scales.reshape(-1)[idx].contiguous()
+    return rows, scales
