@@ -331,3 +331,40 @@ def contiguous_rope(w: Workload):
     if w.spec.dtype == "fp8":
         scales = w.k_rope_scales.reshape(-1)[idx].contiguous()
     return rows, scales
+
+
+KV_LORA_RANK = 512   # latent width of a DeepSeek-V3 MLA cache row (rope dims follow)
+
+
+def latent_cache(w: Workload, kv_lora_rank: int = KV_LORA_RANK):
+    """A paged latent cache for workload `w` (bf16 only): every pool row is
+    [c_kv (kv_lora_rank values) | the workload's 64 K_rope values], placed
+    through w's page table, plus synthetic up-projection weights W_UK, W_UV of
+    shape [H * 128, kv_lora_rank] (nn.Linear layout: output features first).
+
+    Draws from its own generator (seed + 10007).  c_kv ~ value_scale * N(0,1)
+    and weights ~ N(0, 1/kv_lora_rank), so the projected K_nope / V entries
+    have about the spread of c_kv.  Slack slots and the spare page are NaN.
+    Returns (pool [num_pages, P, kv_lora_rank + 64] bf16, w_uk, w_uv)."""
+    assert w.spec.dtype == "bf16", "the latent cache is drawn for bf16 workloads"
+    rng = np.random.Generator(np.random.PCG64(w.spec.seed + 10007))
+    H, P = w.heads, w.page_size
+    Sk = w.total_k
+    c_kv = _normal_bf16(rng, Sk * kv_lora_rank, w.spec.value_scale).view(Sk, kv_lora_rank)
+    std = 1.0 / math.sqrt(kv_lora_rank)
+    w_uk = _normal_bf16(rng, H * NOPE_DEPTH * kv_lora_rank, std).view(H * NOPE_DEPTH, kv_lora_rank)
+    w_uv = _normal_bf16(rng, H * V_DEPTH * kv_lora_rank, std).view(H * V_DEPTH, kv_lora_rank)
+    width = kv_lora_rank + ROPE_DEPTH
+    pool = torch.full((w.num_pages, P, width), float("nan"), dtype=torch.bfloat16)
+    flat = pool.view(-1, width)
+    src = w.k_rope_pool.view(-1, w.k_rope_pool.shape[-1])
+    c0 = w.spec.rope_col
+    g = 0
+    for b in range(w.batch):
+        L = int(w.n[b] + w.prior[b])
+        j = np.arange(L)
+        idx = torch.from_numpy(w.page_table[b, j // P].astype(np.int64) * P + j % P)
+        flat[idx, :kv_lora_rank] = c_kv[g:g + L]
+        flat[idx, kv_lora_rank:] = src[idx, c0:c0 + ROPE_DEPTH]
+        g += L
+    return pool, w_uk, w_uv
