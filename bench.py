@@ -73,6 +73,28 @@ def source_sha1():
         return hashlib.sha1(f.read()).hexdigest()
 
 
+class Ticker:
+    """Labelled segments of the timed steps: tick(label) records an event on
+    the stream that ends the previous segment and starts `label` (None ends
+    without starting one); totals() sums each label's event-timed spans."""
+
+    def __init__(self, stream):
+        self.stream = stream
+        self.marks = []
+
+    def tick(self, label):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(self.stream)
+        self.marks.append((label, e))
+
+    def totals(self):
+        out = {}
+        for (label, e0), (_, e1) in zip(self.marks, self.marks[1:]):
+            if label is not None:
+                out[label] = out.get(label, 0.0) + e0.elapsed_time(e1)
+        return out
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons while the timed region runs."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -227,9 +249,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=[c.name for c in workloads.CONFIGS],
                     help="workload to time (default: the DeepSeek-V3-shaped bf16 batch)")
-    ap.add_argument("--mode", default="full", choices=["full", "chunked", "contiguous"],
-                    help="full-context attention call (paged K_rope), one call per plan buffer row "
-                         "plus the merge, or the full-context call on a contiguous K_rope")
+    ap.add_argument("--mode", default="full", choices=["full", "chunked", "contiguous", "latent"],
+                    help="full-context attention call (paged K_rope); one call per plan buffer row "
+                         "plus the merge; the full-context call on a contiguous K_rope; or the "
+                         "latent-cache path (per row: gather, K/V up-projection, attention; merge)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -251,6 +274,12 @@ def main():
     F = causal_flops(w)
     d = workloads.device_inputs(w, device=dev)
     contiguous = args.mode == "contiguous"
+    latent = args.mode == "latent"
+    if latent:
+        assert not fp8, "the latent-cache path is bf16"
+        lpool, w_uk, w_uv = workloads.latent_cache(w)
+        d["latent_pool"], d["w_uk"], d["w_uv"] = lpool.to(dev), w_uk.to(dev), w_uv.to(dev)
+        del d["k_nope"], d["v"], d["k_rope_pool"]
     if contiguous:
         rows, rsc = workloads.contiguous_rope(w)
         d["k_rope_contig"] = rows[:, spec.rope_col:spec.rope_col + 64].contiguous().to(dev)
@@ -270,12 +299,14 @@ def main():
                 torch.empty((R,), dtype=torch.int32, device=dev),
                 torch.empty((1,), dtype=torch.int32, device=dev))
     stream = torch.cuda.current_stream(dev)
-    chunked = args.mode == "chunked"
+    chunked = args.mode in ("chunked", "latent")
     scratch = binding.chunked_scratch(R, Tq, H, dev) if chunked else None
+    lbuf = binding.LatentRowBuffers(T, 576, H, dev) if latent else None
 
-    def attention(inp, o, mark=None):
-        """The attention part of a step; `mark` (an event) is recorded between
-        the per-row calls and the merge in chunked mode."""
+    def attention(inp, o, tk=None):
+        """The attention part of a step; `tk` (a Ticker) labels its segments."""
+        tick = tk.tick if tk is not None else (lambda label: None)
+        tick("attn")
         if contiguous:
             binding.prefill_ragged_contiguous(o, inp["q"], inp["k_nope"], inp["v"], inp["k_rope_contig"],
                                               inp["row_offsets"], inp["cache_lens"], w.scale,
@@ -289,12 +320,27 @@ def main():
         po, pl = scratch
         for r in range(R):
             lo, hi = r * T, min((r + 1) * T, w.total_k)
+            if latent:
+                # Gather the row's latent rows, project K_nope and V, attend.
+                n = hi - lo
+                rows = lbuf.rows[:n]
+                tick("gather")
+                binding.gather_rows(rows, inp["latent_pool"], inp["page_table"], plan_out[0][r],
+                                    plan_out[1][r], stream=stream)
+                tick("gemm")
+                kn, vv = lbuf.k_nope[:n], lbuf.v[:n]
+                binding.up_project(kn.view(n, H * 128), rows[:, :512], inp["w_uk"], lbuf.gemm_ws, stream)
+                binding.up_project(vv.view(n, H * 128), rows[:, :512], inp["w_uv"], lbuf.gemm_ws, stream)
+                tick("attn")
+                binding.prefill_ragged_chunk_contiguous(
+                    po[r], pl[r], inp["q"], kn, vv, rows[:, 512:576], inp["row_offsets"], inp["cache_lens"],
+                    plan_out[0][r], plan_out[1][r], w.scale, binding.MLA_MASK_CAUSAL, ws, stream=stream)
+                continue
             binding.prefill_ragged_chunk(po[r], pl[r], inp["q"], inp["k_nope"][lo:hi], inp["v"][lo:hi],
                                          inp["k_rope_pool"], inp["page_table"], inp["row_offsets"],
                                          inp["cache_lens"], plan_out[0][r], plan_out[1][r], w.scale,
                                          binding.MLA_MASK_CAUSAL, ws, stream=stream, **scales)
-        if mark is not None:
-            mark.record(stream)
+        tick("merge")
         binding.merge(o, po, pl, inp["row_offsets"], plan_out[0], stream=stream)
 
     def step(inp, o):
@@ -305,38 +351,44 @@ def main():
         step(d, out)
     assert binding.device_status(ws) == 0, "device status after warm-up"
 
-    # Device-resident timing: per-step events around the attention call and
-    # around the whole step, on the launching stream.
-    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
+    # Device-resident timing: labelled segments of every step (events on the
+    # launching stream) and the whole timed region.
+    tk = Ticker(stream)
     barrier(world)
     with ClockSampler(local) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for i in range(args.steps):
-            ev[i][0].record(stream)
+            tk.tick("plan")
             binding.plan(d["row_offsets"], d["cache_lens"], T, R, stream=stream, out=plan_out)
-            ev[i][1].record(stream)
-            attention(d, out, mark=ev[i][2] if chunked else None)
-            ev[i][3].record(stream)
+            attention(d, out, tk)
+            tk.tick(None)
         t_end.record(stream)
         barrier(world)
     total_ms = dist_max(t_start.elapsed_time(t_end), world)
     # Attention-kernel span (the per-row calls in chunked mode) and merge span.
-    attn_ms = statistics.mean(e[1].elapsed_time(e[2] if chunked else e[3]) for e in ev)
-    merge_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) if chunked else None
+    seg = {k: v / args.steps for k, v in tk.totals().items()}   # ms per step per segment
+    attn_ms = seg["attn"]
+    merge_ms = seg.get("merge")
     assert binding.device_status(ws) == 0, "device status after timed steps"
     clocks = clk.summary()
 
     # End to end through the public API: pinned host inputs -> device, plan +
     # attention, output -> pinned host, every step.
     h = workloads.device_inputs(w, device="cpu", pin=True)
+    if latent:
+        for k in ("latent_pool", "w_uk", "w_uv"):
+            h[k] = d[k].cpu().pin_memory()
     if contiguous:
         h["k_rope_contig"] = d["k_rope_contig"].cpu().pin_memory()
         if fp8:
             h["k_rope_scales"] = d["k_rope_scales"].cpu().pin_memory()
-    keys = ["q", "k_nope", "v", "row_offsets", "cache_lens"]
-    keys += ["k_rope_contig"] if contiguous else ["k_rope_pool", "page_table"]
+    keys = ["q", "row_offsets", "cache_lens"]
+    if latent:
+        keys += ["latent_pool", "page_table", "w_uk", "w_uv"]
+    else:
+        keys += ["k_nope", "v"] + (["k_rope_contig"] if contiguous else ["k_rope_pool", "page_table"])
     if fp8:
         keys += ["q_scale", "k_scale", "v_scale", "k_rope_scales"]
     d2 = {k: torch.empty_like(d[k]) for k in keys}
@@ -382,9 +434,22 @@ def main():
         merge_roofline = {"bound": "hbm", "achieved": m_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                           "frac": m_gbs / peaks["hbm_gbs"], "bytes_per_launch": mbytes,
                           "ms": merge_ms, "kernel": "merge_kernel"}
+    latent_rooflines = None
+    if latent:
+        # Up-projection: two GEMMs [S, 512] x [512, H*128]; gather: every
+        # context row's 1152 bytes read once and written once.
+        gflop = 2 * 2 * w.total_k * 512 * H * 128
+        g_tf = gflop / (seg["gemm"] * 1e-3) / 1e12
+        gb = 2 * w.total_k * 576 * 2
+        latent_rooflines = {
+            "gemm": {"bound": "tensor", "achieved": g_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": g_tf / peaks["bf16_tflops"], "ms": seg["gemm"], "kernel": "cuBLASLt (library)"},
+            "gather": {"bound": "hbm", "achieved": gb / (seg["gather"] * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                       "unit": "GB/s", "frac": gb / (seg["gather"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                       "ms": seg["gather"], "kernel": "gather_kernel", "bytes_per_step": gb}}
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not latent:
         rows, nh = oracle_shape_for(w, 12.0)
         f, dt, sample = oracle_sample(w, rows, list(range(nh)))
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
@@ -401,7 +466,10 @@ def main():
                        "total_q_tokens": Tq, "heads": H, "causal_effective_tflop_per_step": F / 1e12,
                        "parallelism": f"dp{world} (independent batches)" if world > 1 else "none",
                        "l2": f"inputs ({in_bytes / 1e9:.2f} GB) larger than L2; no flush",
-                       "step": ("mla_prefill_plan + %d x mla_prefill_ragged_chunk (T=%d) + mla_prefill_merge"
+                       "step": ("mla_prefill_plan + %d x (mla_gather_rows + 2 x mla_up_project + "
+                                "mla_prefill_ragged_chunk_contiguous) (T=%d) + mla_prefill_merge" % (R, T))
+                               if latent else
+                               ("mla_prefill_plan + %d x mla_prefill_ragged_chunk (T=%d) + mla_prefill_merge"
                                 % (R, T)) if chunked else
                                ("mla_prefill_plan + mla_prefill_ragged_contiguous (K_rope [S_k, 64], not paged)"
                                 if contiguous else "mla_prefill_plan + mla_prefill_ragged")},
@@ -409,7 +477,8 @@ def main():
             "clocks": clocks,
             "e2e": {"value": world * F * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": ((2 + R * (3 if fp8 else 2)) if chunked else (4 if fp8 else 3)) * args.steps,
+            "gpu_launches": ((2 + 3 * R) if latent else (2 + R * (3 if fp8 else 2)) if chunked
+                             else (4 if fp8 else 3)) * args.steps,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                          "kernel": ("mla_attention_kernel over %d buffer rows (+ their scheduler launches)" % R)
@@ -419,6 +488,10 @@ def main():
         }
         if chunked:
             line["roofline_merge"] = merge_roofline
+        if latent:
+            line["roofline_gemm"] = latent_rooflines["gemm"]
+            line["roofline_gather"] = latent_rooflines["gather"]
+            line["segments_ms"] = seg
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

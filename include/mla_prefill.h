@@ -288,6 +288,64 @@ mla_status_t mla_prefill_merge(const mla_tensor_t* out, const mla_tensor_t* part
                                const uint32_t* buffer_row_offsets, uint32_t batch,
                                mla_stream_t stream);
 
+/*
+ * mla_prefill_ragged_chunk with a contiguous K_rope for the row (the
+ * flare_mla_prefill overload with a plain k_rope tensor): k_rope is
+ * [S_row, 64], row t holding the rope dims of the row's K buffer position t
+ * (for example the last 64 columns of rows gathered by mla_gather_rows), so no
+ * page table is read.  batch gives B; fp8 K_rope takes one scale per row and
+ * the workspace then needs mla_prefill_ragged_workspace_size_fp8(B, S_row).
+ * Everything else as mla_prefill_ragged_chunk.
+ */
+mla_status_t mla_prefill_ragged_chunk_contiguous(
+    const mla_tensor_t* out, const mla_tensor_t* lse, const mla_tensor_t* q, const mla_tensor_t* k_nope,
+    const mla_tensor_t* v, const mla_tensor_t* k_rope, const uint32_t* row_offsets,
+    const uint32_t* cache_lens, const uint32_t* buffer_row_offsets, const uint32_t* cache_offsets,
+    uint32_t batch, float scale, mla_mask_t mask, void* workspace, size_t workspace_bytes,
+    mla_stream_t stream);
+
+/*
+ * Gather of one buffer row out of a paged cache into a contiguous buffer
+ * (generic_flare_mla_prefill_ragged_paged_plan summary: the plan exists so the
+ * prefill kernel "can gather K/V entries into a contiguous buffer"; Args:
+ * buffer_row_offsets, cache_offsets).  For every sequence b and
+ * 0 <= i < buffer_row_offsets[b+1] - buffer_row_offsets[b], with context
+ * position a = cache_offsets[b] + i:
+ *   dst[buffer_row_offsets[b] + i, :] = cache[page_table[b, a / P], a % P, :]
+ *   dst          device [rows, W] (written for positions < min(rows,
+ *                buffer_row_offsets[B]) only); same dtype as cache
+ *   cache        device [num_pages, P, W], bf16 or fp8 (codes copied as
+ *                bytes), W * element size a multiple of 16 bytes; e.g. a
+ *                DeepSeek-V3 latent cache row [c_kv 512 | k_rope 64]
+ *   page_table   device uint32 [B, max_pages]
+ *   buffer_row_offsets, cache_offsets  one row of the plan ([B+1], [B])
+ *   status       device uint32 or NULL: an out-of-range page id or
+ *                page-table column skips that row chunk and ORs
+ *                MLA_DEVICE_STATUS_BAD_PAGE / _BAD_COLUMN into *status
+ * One launch, HBM-bound; no host synchronisation.
+ */
+mla_status_t mla_gather_rows(const mla_tensor_t* dst, const mla_tensor_t* cache,
+                             const mla_tensor_t* page_table, const uint32_t* buffer_row_offsets,
+                             const uint32_t* cache_offsets, uint32_t* status, mla_stream_t stream);
+
+/*
+ * Up-projection of latent rows (the step between the gather and the
+ * attention when K_nope and V are not cached; the weights are the caller's):
+ *   out[t, n] = sum_k latent[t, k] * weight[n, k]
+ *   out     device bf16 [rows, N] (e.g. K_nope [rows, H, 128] viewed as
+ *           [rows, H * 128])
+ *   latent  device bf16 [rows, K] (row stride may exceed K: the c_kv
+ *           columns of gathered latent rows)
+ *   weight  device bf16 [N, K] (nn.Linear layout)
+ *   workspace / workspace_bytes  device scratch for the GEMM (0 allowed;
+ *           32 MiB lets the library pick its fastest kernels)
+ * Rows of every operand must start 16-byte aligned.  A plain dense GEMM run
+ * through cuBLASLt (fp32 accumulation, bf16 output).
+ */
+mla_status_t mla_up_project(const mla_tensor_t* out, const mla_tensor_t* latent,
+                            const mla_tensor_t* weight, void* workspace, size_t workspace_bytes,
+                            mla_stream_t stream);
+
 /* Device status bits written into the workspace's first uint32. */
 #define MLA_DEVICE_STATUS_BAD_PAGE 0x1u    /* page id >= num_pages */
 #define MLA_DEVICE_STATUS_BAD_COLUMN 0x2u  /* context needs more pages than max_pages */

@@ -22,6 +22,7 @@ STATUS_BITS = {0x1: "BAD_PAGE", 0x2: "BAD_COLUMN", 0x4: "BAD_OFFSETS", 0x8: "TIM
 EXPORTS = ["mla_prefill_plan", "mla_prefill_plan_max_rows", "mla_prefill_ragged_workspace_size",
            "mla_prefill_ragged_workspace_size_fp8", "mla_prefill_ragged", "mla_prefill_ragged_noalloc",
            "mla_prefill_ragged_chunk", "mla_prefill_merge", "mla_prefill_ragged_contiguous",
+           "mla_prefill_ragged_chunk_contiguous", "mla_gather_rows", "mla_up_project",
            "mla_read_device_status",
            "mla_last_error_string"]
 
@@ -73,6 +74,14 @@ def load(path=LIB_PATH):
     lib.mla_prefill_ragged_contiguous.argtypes = [pt, pt, pt, pt, pt, vp, vp, u32, ctypes.c_float,
                                                   ctypes.c_int, vp, ctypes.c_size_t, vp]
     lib.mla_prefill_ragged_contiguous.restype = ctypes.c_int
+    lib.mla_prefill_ragged_chunk_contiguous.argtypes = [pt, pt, pt, pt, pt, pt, vp, vp, vp, vp, u32,
+                                                        ctypes.c_float, ctypes.c_int, vp,
+                                                        ctypes.c_size_t, vp]
+    lib.mla_prefill_ragged_chunk_contiguous.restype = ctypes.c_int
+    lib.mla_gather_rows.argtypes = [pt, pt, pt, vp, vp, vp, vp]
+    lib.mla_gather_rows.restype = ctypes.c_int
+    lib.mla_up_project.argtypes = [pt, pt, pt, vp, ctypes.c_size_t, vp]
+    lib.mla_up_project.restype = ctypes.c_int
     lib.mla_read_device_status.argtypes = [vp, ctypes.POINTER(u32), vp]
     lib.mla_read_device_status.restype = ctypes.c_int
     lib.mla_last_error_string.argtypes = []
@@ -243,6 +252,85 @@ def prefill_ragged_contiguous(out, q, k_nope, v, k_rope, row_offsets, cache_lens
                                              _ptr(cache_lens), B, float(scale), int(mask),
                                              _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
+
+
+def prefill_ragged_chunk_contiguous(out, lse, q, k_nope, v, k_rope, row_offsets, cache_lens,
+                                    buffer_row_offsets, cache_offsets, scale, mask=MLA_MASK_CAUSAL,
+                                    workspace=None, q_scale=None, k_scale=None, v_scale=None,
+                                    k_rope_scales=None, stream=None):
+    """mla_prefill_ragged_chunk_contiguous: one buffer row whose K_rope is the
+    row's own [S_row, 64] tensor (row t = buffer position t)."""
+    lib = load()
+    B = row_offsets.numel() - 1
+    fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
+    if workspace is None:
+        workspace = alloc_workspace(B, q.device, k_rope.shape[0] if fp8 else None)
+    gran_t = MLA_SCALE_PER_TENSOR if fp8 else MLA_SCALE_NONE
+    d_out, d_lse = describe(out, MLA_DTYPE_BF16), describe(lse, MLA_DTYPE_F32)
+    d_q = describe(q, _dtype_code(q), q_scale if fp8 else None, gran_t)
+    d_k = describe(k_nope, _dtype_code(k_nope), k_scale if fp8 else None, gran_t)
+    d_v = describe(v, _dtype_code(v), v_scale if fp8 else None, gran_t)
+    d_r = describe(k_rope, _dtype_code(k_rope), k_rope_scales if fp8 else None,
+                   MLA_SCALE_PER_TOKEN if fp8 else MLA_SCALE_NONE)
+    _check(lib.mla_prefill_ragged_chunk_contiguous(
+        ctypes.byref(d_out), ctypes.byref(d_lse), ctypes.byref(d_q), ctypes.byref(d_k), ctypes.byref(d_v),
+        ctypes.byref(d_r), _ptr(row_offsets), _ptr(cache_lens), _ptr(buffer_row_offsets),
+        _ptr(cache_offsets), B, float(scale), int(mask), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+    return out, lse
+
+
+def gather_rows(dst, cache, page_table, buffer_row_offsets, cache_offsets, status=None, stream=None):
+    """mla_gather_rows: dst[bro[b] + i] = cache row of context token co[b] + i of sequence b."""
+    code = _dtype_code(cache)
+    d_dst, d_cache = describe(dst, code), describe(cache, code)
+    d_pt = describe(page_table, MLA_DTYPE_U32)
+    _check(load().mla_gather_rows(ctypes.byref(d_dst), ctypes.byref(d_cache), ctypes.byref(d_pt),
+                                  _ptr(buffer_row_offsets), _ptr(cache_offsets), _ptr(status),
+                                  _stream(stream)))
+    return dst
+
+
+GEMM_WORKSPACE_BYTES = 32 << 20
+
+
+def up_project(out, latent, weight, workspace=None, stream=None):
+    """mla_up_project: out [rows, N] = latent [rows, K] x weight [N, K]^T (bf16)."""
+    if workspace is None:
+        workspace = torch.empty(GEMM_WORKSPACE_BYTES, dtype=torch.uint8, device=out.device)
+    d_out = describe(out, MLA_DTYPE_BF16)
+    d_lat = describe(latent, MLA_DTYPE_BF16)
+    d_w = describe(weight, MLA_DTYPE_BF16)
+    _check(load().mla_up_project(ctypes.byref(d_out), ctypes.byref(d_lat), ctypes.byref(d_w),
+                                 _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+class LatentRowBuffers:
+    """Per-row scratch of the latent path: the gathered rows [T, width] and the
+    projected K_nope / V [T, H, 128]."""
+    def __init__(self, T, width, heads, device="cuda"):
+        self.rows = torch.empty((T, width), dtype=torch.bfloat16, device=device)
+        self.k_nope = torch.empty((T, heads, 128), dtype=torch.bfloat16, device=device)
+        self.v = torch.empty((T, heads, 128), dtype=torch.bfloat16, device=device)
+        self.gemm_ws = torch.empty(GEMM_WORKSPACE_BYTES, dtype=torch.uint8, device=device)
+
+
+def prefill_latent_row(po, pl, q, cache, page_table, row_offsets, cache_lens, bro_r, co_r, w_uk,
+                       w_uv, scale, buffers, rows_in_row, mask=MLA_MASK_CAUSAL, workspace=None,
+                       status=None, kv_lora_rank=512, stream=None):
+    """One buffer row from the paged latent cache: gather its rows, up-project
+    K_nope and V, then the row's attention with the gathered K_rope columns."""
+    n = int(rows_in_row)
+    rows = buffers.rows[:n]
+    gather_rows(rows, cache, page_table, bro_r, co_r, status, stream)
+    H = q.shape[1]
+    kn, v = buffers.k_nope[:n], buffers.v[:n]
+    up_project(kn.view(n, H * 128), rows[:, :kv_lora_rank], w_uk, buffers.gemm_ws, stream)
+    up_project(v.view(n, H * 128), rows[:, :kv_lora_rank], w_uv, buffers.gemm_ws, stream)
+    return prefill_ragged_chunk_contiguous(po, pl, q, kn, v, rows[:, kv_lora_rank:kv_lora_rank + 64],
+                                           row_offsets, cache_lens, bro_r, co_r, scale, mask,
+                                           workspace, stream=stream)
 
 
 def merge(out, partial_out, partial_lse, row_offsets, buffer_row_offsets, stream=None):

@@ -1342,6 +1342,18 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
                       nullptr, nullptr, scale, mask, workspace, workspace_bytes, stream);
 }
 
+extern "C" mla_status_t mla_prefill_ragged_chunk_contiguous(
+    const mla_tensor_t* out, const mla_tensor_t* lse, const mla_tensor_t* q, const mla_tensor_t* k_nope,
+    const mla_tensor_t* v, const mla_tensor_t* k_rope, const uint32_t* row_offsets,
+    const uint32_t* cache_lens, const uint32_t* buffer_row_offsets, const uint32_t* cache_offsets,
+    uint32_t batch, float scale, mla_mask_t mask, void* workspace, size_t workspace_bytes,
+    mla_stream_t stream) {
+  if (!buffer_row_offsets) return mla::fail(MLA_ERR_INVALID_ARG, "buffer_row_offsets is NULL");
+  if (batch < 1) return mla::fail(MLA_ERR_INVALID_ARG, "batch must be >= 1");
+  return mla::prefill(out, lse, q, k_nope, v, k_rope, nullptr, batch, row_offsets, cache_lens,
+                      buffer_row_offsets, cache_offsets, scale, mask, workspace, workspace_bytes, stream);
+}
+
 extern "C" mla_status_t mla_prefill_ragged_contiguous(const mla_tensor_t* out, const mla_tensor_t* q,
                                                       const mla_tensor_t* k_nope, const mla_tensor_t* v,
                                                       const mla_tensor_t* k_rope,

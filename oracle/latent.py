@@ -44,12 +44,20 @@ def gather_row(pool, page_table, buffer_row_offsets, cache_offsets, page_size):
     return out
 
 
-def up_project(c_kv, weight):
-    """[n, 512] x W[H*128, 512] -> [n, H, 128] (one float64 matmul)."""
-    wt = decode_bf16(weight.view(torch.int16).numpy().view(np.uint16)) if isinstance(weight, torch.Tensor) \
-        else np.asarray(weight, dtype=np.float64)
-    n = c_kv.shape[0]
-    return (c_kv @ wt.T).reshape(n, -1, 128)
+def up_project(c_kv, weight, heads=None):
+    """[n, 512] x W[H*128, 512] -> [n, H, 128] (float64 matmuls); with
+    `heads`, only those heads' output columns are computed (the others are NaN)."""
+    if isinstance(weight, torch.Tensor):
+        weight = weight.view(torch.int16).numpy().view(np.uint16)
+        wt = None
+    else:
+        wt = np.asarray(weight, dtype=np.float64)
+    n, H = c_kv.shape[0], weight.shape[0] // 128
+    out = np.full((n, H, 128), np.nan, dtype=np.float64)
+    for h in (range(H) if heads is None else heads):
+        wh = wt[h * 128:(h + 1) * 128] if wt is not None else decode_bf16(weight[h * 128:(h + 1) * 128])
+        out[:, h, :] = c_kv @ wh.T
+    return out
 
 
 def context_latent(w, pool, b):
@@ -78,8 +86,8 @@ def reference(w, pool, w_uk, w_uv, heads=None, rows=None, kv_lora_rank=512):
         if n == 0 or sel.size == 0:
             continue
         lat = context_latent(w, pool, b)
-        k_nope = up_project(lat[:, :kv_lora_rank], w_uk)
-        v = up_project(lat[:, :kv_lora_rank], w_uv)
+        k_nope = up_project(lat[:, :kv_lora_rank], w_uk, heads)
+        v = up_project(lat[:, :kv_lora_rank], w_uv, heads)
         rope = lat[:, kv_lora_rank:kv_lora_rank + ROPE]
         q0 = int(w.row_offsets[b])
         j = np.arange(L)

@@ -213,3 +213,32 @@ def test_contiguous_rejects_bad_arguments(lib, case):
                                            a["ws_bytes"], None)
     assert st == binding.MLA_ERR_INVALID_ARG
     assert lib.mla_last_error_string()
+
+
+def test_gather_rejects_bad_arguments(lib):
+    r = ctypes.byref
+    dst, cache = _desc([8, 576]), _desc([4, 16, 576])
+    pt = _desc([2, 2], binding.MLA_DTYPE_U32)
+    f = lib.mla_gather_rows
+    ok = binding.MLA_ERR_INVALID_ARG
+    assert f(r(_desc([8, 512])), r(cache), r(pt), 0x60000, 0x70000, None, None) == ok   # width
+    assert f(r(dst), r(_desc([4, 16, 12])), r(pt), 0x60000, 0x70000, None, None) == ok  # 24-byte rows
+    assert f(r(dst), r(cache), r(pt), None, 0x70000, None, None) == ok
+    assert f(r(dst), r(cache), r(pt), 0x60000, None, None, None) == ok
+    assert f(r(dst), r(cache), r(_desc([2, 2])), 0x60000, 0x70000, None, None) == ok  # table dtype
+    assert f(r(dst), r(_desc([4, 16, 576], binding.MLA_DTYPE_U32)), r(pt), 0x60000, 0x70000, None,
+             None) == ok
+
+
+def test_up_project_rejects_bad_arguments(lib):
+    r = ctypes.byref
+    f = lib.mla_up_project
+    bad = binding.MLA_ERR_INVALID_ARG
+    out, lat, wt = _desc([8, 256]), _desc([8, 512]), _desc([256, 512])
+    assert f(r(_desc([8, 128])), r(lat), r(wt), None, 0, None) == bad       # N mismatch
+    assert f(r(out), r(_desc([8, 500])), r(wt), None, 0, None) == bad       # K mismatch
+    assert f(r(out), r(lat), r(_desc([256, 512], binding.MLA_DTYPE_F32)), None, 0, None) == bad
+    assert f(r(out), r(lat), r(wt), None, 1024, None) == bad                # workspace NULL
+    odd = _desc([8, 512])
+    odd.stride[0] = 516                                                     # 1032-byte rows
+    assert f(r(out), r(odd), r(wt), None, 0, None) == bad
