@@ -249,6 +249,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=[c.name for c in workloads.CONFIGS],
                     help="workload to time (default: the DeepSeek-V3-shaped bf16 batch)")
+    ap.add_argument("--combine", default="fold", choices=["fold", "merge"],
+                    help="chunked / latent modes: fold every row into the output in place "
+                         "(MLA_CHUNK_ACCUMULATE), or write per-row outputs and run mla_prefill_merge")
     ap.add_argument("--mode", default="full", choices=["full", "chunked", "contiguous", "latent"],
                     help="full-context attention call (paged K_rope); one call per plan buffer row "
                          "plus the merge; the full-context call on a contiguous K_rope; or the "
@@ -300,7 +303,9 @@ def main():
                 torch.empty((1,), dtype=torch.int32, device=dev))
     stream = torch.cuda.current_stream(dev)
     chunked = args.mode in ("chunked", "latent")
-    scratch = binding.chunked_scratch(R, Tq, H, dev) if chunked else None
+    fold = chunked and args.combine == "fold"
+    scratch = binding.chunked_scratch(R, Tq, H, dev) if chunked and not fold else None
+    lse_buf = torch.empty((Tq, H), dtype=torch.float32, device=dev) if fold else None
     lbuf = binding.LatentRowBuffers(T, 576, H, dev) if latent else None
 
     def attention(inp, o, tk=None):
@@ -317,9 +322,10 @@ def main():
                                    inp["page_table"], inp["row_offsets"], inp["cache_lens"], w.scale,
                                    binding.MLA_MASK_CAUSAL, ws, stream=stream, **scales)
             return
-        po, pl = scratch
+        flags = binding.MLA_CHUNK_ACCUMULATE if fold else 0
         for r in range(R):
             lo, hi = r * T, min((r + 1) * T, w.total_k)
+            o_r, l_r = (o, lse_buf) if fold else (scratch[0][r], scratch[1][r])
             if latent:
                 # Gather the row's latent rows, project K_nope and V, attend.
                 n = hi - lo
@@ -333,15 +339,17 @@ def main():
                 binding.up_project(vv.view(n, H * 128), rows[:, :512], inp["w_uv"], lbuf.gemm_ws, stream)
                 tick("attn")
                 binding.prefill_ragged_chunk_contiguous(
-                    po[r], pl[r], inp["q"], kn, vv, rows[:, 512:576], inp["row_offsets"], inp["cache_lens"],
-                    plan_out[0][r], plan_out[1][r], w.scale, binding.MLA_MASK_CAUSAL, ws, stream=stream)
+                    o_r, l_r, inp["q"], kn, vv, rows[:, 512:576], inp["row_offsets"], inp["cache_lens"],
+                    plan_out[0][r], plan_out[1][r], w.scale, binding.MLA_MASK_CAUSAL, ws, stream=stream,
+                    flags=flags)
                 continue
-            binding.prefill_ragged_chunk(po[r], pl[r], inp["q"], inp["k_nope"][lo:hi], inp["v"][lo:hi],
+            binding.prefill_ragged_chunk(o_r, l_r, inp["q"], inp["k_nope"][lo:hi], inp["v"][lo:hi],
                                          inp["k_rope_pool"], inp["page_table"], inp["row_offsets"],
                                          inp["cache_lens"], plan_out[0][r], plan_out[1][r], w.scale,
-                                         binding.MLA_MASK_CAUSAL, ws, stream=stream, **scales)
-        tick("merge")
-        binding.merge(o, po, pl, inp["row_offsets"], plan_out[0], stream=stream)
+                                         binding.MLA_MASK_CAUSAL, ws, stream=stream, flags=flags, **scales)
+        if not fold:
+            tick("merge")
+            binding.merge(o, scratch[0], scratch[1], inp["row_offsets"], plan_out[0], stream=stream)
 
     def step(inp, o):
         binding.plan(inp["row_offsets"], inp["cache_lens"], T, R, stream=stream, out=plan_out)
@@ -424,7 +432,7 @@ def main():
     if ATTENTION_TRAFFIC["source_sha1"] == source_sha1() and args.mode == "full":
         traffic = ATTENTION_TRAFFIC["bytes_per_launch"].get(spec.name)
     merge_roofline = None
-    if chunked:
+    if chunked and not fold:
         # Algorithmic merge bytes: per (token, head), 256 + 4 bytes read from
         # each row holding keys of its sequence, 256 bytes written.
         G = np.concatenate([[0], np.cumsum(w.n + w.prior)])
@@ -455,6 +463,16 @@ def main():
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
                "sample": sample + f"; {dt:.1f} s of float64 numpy on the host"}
 
+    # This library's kernels per step (cuBLASLt's GEMM kernels not counted).
+    if latent:
+        launches_per_step = 1 + 3 * R          # plan; per row gather, scheduler, attention
+    elif chunked:
+        launches_per_step = 1 + R * (3 if fp8 else 2)
+    else:
+        launches_per_step = 4 if fp8 else 3
+    if chunked and not fold:
+        launches_per_step += 1                 # merge
+    merge_txt = "" if fold else " + mla_prefill_merge"
     if rank == 0:
         value = world * F * args.steps / (total_ms * 1e-3) / 1e12
         line = {
@@ -467,18 +485,17 @@ def main():
                        "parallelism": f"dp{world} (independent batches)" if world > 1 else "none",
                        "l2": f"inputs ({in_bytes / 1e9:.2f} GB) larger than L2; no flush",
                        "step": ("mla_prefill_plan + %d x (mla_gather_rows + 2 x mla_up_project + "
-                                "mla_prefill_ragged_chunk_contiguous) (T=%d) + mla_prefill_merge" % (R, T))
+                                "mla_prefill_ragged_chunk_contiguous) (T=%d)%s" % (R, T, merge_txt))
                                if latent else
-                               ("mla_prefill_plan + %d x mla_prefill_ragged_chunk (T=%d) + mla_prefill_merge"
-                                % (R, T)) if chunked else
+                               ("mla_prefill_plan + %d x mla_prefill_ragged_chunk (T=%d)%s"
+                                % (R, T, merge_txt)) if chunked else
                                ("mla_prefill_plan + mla_prefill_ragged_contiguous (K_rope [S_k, 64], not paged)"
                                 if contiguous else "mla_prefill_plan + mla_prefill_ragged")},
             "pct_of_peak": 100.0 * value / world / peak,
             "clocks": clocks,
             "e2e": {"value": world * F * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": ((2 + 3 * R) if latent else (2 + R * (3 if fp8 else 2)) if chunked
-                             else (4 if fp8 else 3)) * args.steps,
+            "gpu_launches": launches_per_step * args.steps,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                          "kernel": ("mla_attention_kernel over %d buffer rows (+ their scheduler launches)" % R)
@@ -487,6 +504,8 @@ def main():
             "cpu_baseline": cpu,
         }
         if chunked:
+            line["config"]["combine"] = "in-place fold (MLA_CHUNK_ACCUMULATE)" if fold else "mla_prefill_merge"
+        if merge_roofline is not None:
             line["roofline_merge"] = merge_roofline
         if latent:
             line["roofline_gemm"] = latent_rooflines["gemm"]

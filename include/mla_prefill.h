@@ -246,7 +246,18 @@ mla_status_t mla_prefill_ragged_noalloc(const mla_tensor_t* out, const mla_tenso
  *     lse[t, h] = ln sum_j exp(s_j) over the same keys (natural log, s_j the
  *     scaled scores; fp8 scores include the dequantisation scales);
  *   - a query that sees no key of the row gets out = 0 and lse = -inf;
- *   - rows of sequences with W_b = 0 are not written (neither out nor lse).
+ *   - rows of sequences with W_b = 0 are not written (neither out nor lse);
+ *   - flags = MLA_CHUNK_ACCUMULATE folds the row into out / lse instead of
+ *     overwriting them: for a sequence whose window starts after context
+ *     position 0 (cache_offsets[b] > 0), out and lse must hold the result
+ *     over its earlier positions (the earlier rows' calls, made in row
+ *     order with this flag), and the call leaves the combination
+ *       lse' = ln(e^lse + e^lse_row),
+ *       out' = (e^lse out + e^lse_row out_row) / (e^lse + e^lse_row);
+ *     a sequence whose window starts at position 0 is written afresh.  After
+ *     the last row, out is the full-context result and lse its log-sum-exp,
+ *     with no mla_prefill_merge and no per-row buffers.  flags = 0 writes the
+ *     row's own result.
  *   lse          device float32 [Tq, H] (written), 4-byte aligned
  *   k_nope, v    device [S_row, H, 128] with S_row >= buffer_row_offsets[B] >= 1
  *   buffer_row_offsets  device uint32 [B+1], non-decreasing
@@ -261,7 +272,10 @@ mla_status_t mla_prefill_ragged_chunk(const mla_tensor_t* out, const mla_tensor_
                                       const mla_tensor_t* page_table, const uint32_t* row_offsets,
                                       const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
                                       const uint32_t* cache_offsets, float scale, mla_mask_t mask,
-                                      void* workspace, size_t workspace_bytes, mla_stream_t stream);
+                                      uint32_t flags, void* workspace, size_t workspace_bytes,
+                                      mla_stream_t stream);
+
+#define MLA_CHUNK_ACCUMULATE 0x1u /* mla_prefill_ragged_chunk*: fold into out / lse */
 
 /*
  * Combines the rows of a chunked execution (the pages give only the per-row
@@ -301,8 +315,8 @@ mla_status_t mla_prefill_ragged_chunk_contiguous(
     const mla_tensor_t* out, const mla_tensor_t* lse, const mla_tensor_t* q, const mla_tensor_t* k_nope,
     const mla_tensor_t* v, const mla_tensor_t* k_rope, const uint32_t* row_offsets,
     const uint32_t* cache_lens, const uint32_t* buffer_row_offsets, const uint32_t* cache_offsets,
-    uint32_t batch, float scale, mla_mask_t mask, void* workspace, size_t workspace_bytes,
-    mla_stream_t stream);
+    uint32_t batch, float scale, mla_mask_t mask, uint32_t flags, void* workspace,
+    size_t workspace_bytes, mla_stream_t stream);
 
 /*
  * Gather of one buffer row out of a paged cache into a contiguous buffer

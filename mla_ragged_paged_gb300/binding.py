@@ -16,6 +16,7 @@ MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, 1, 2, 3
 MLA_DTYPE_BF16, MLA_DTYPE_FP8_E4M3, MLA_DTYPE_U32, MLA_DTYPE_F32 = 0, 1, 2, 3
 MLA_MASK_CAUSAL, MLA_MASK_NULL = 0, 1
 MLA_SCALE_NONE, MLA_SCALE_PER_TENSOR, MLA_SCALE_PER_TOKEN = 0, 1, 2
+MLA_CHUNK_ACCUMULATE = 0x1
 STATUS_BITS = {0x1: "BAD_PAGE", 0x2: "BAD_COLUMN", 0x4: "BAD_OFFSETS", 0x8: "TIMEOUT"}
 
 # Names exported by the C ABI (kept in step with include/mla_prefill.h).
@@ -67,7 +68,7 @@ def load(path=LIB_PATH):
                                                ctypes.c_int, vp]
     lib.mla_prefill_ragged_noalloc.restype = ctypes.c_int
     lib.mla_prefill_ragged_chunk.argtypes = [pt, pt, pt, pt, pt, pt, pt, vp, vp, vp, vp, ctypes.c_float,
-                                             ctypes.c_int, vp, ctypes.c_size_t, vp]
+                                             ctypes.c_int, u32, vp, ctypes.c_size_t, vp]
     lib.mla_prefill_ragged_chunk.restype = ctypes.c_int
     lib.mla_prefill_merge.argtypes = [pt, pt, pt, vp, vp, u32, vp]
     lib.mla_prefill_merge.restype = ctypes.c_int
@@ -75,7 +76,7 @@ def load(path=LIB_PATH):
                                                   ctypes.c_int, vp, ctypes.c_size_t, vp]
     lib.mla_prefill_ragged_contiguous.restype = ctypes.c_int
     lib.mla_prefill_ragged_chunk_contiguous.argtypes = [pt, pt, pt, pt, pt, pt, vp, vp, vp, vp, u32,
-                                                        ctypes.c_float, ctypes.c_int, vp,
+                                                        ctypes.c_float, ctypes.c_int, u32, vp,
                                                         ctypes.c_size_t, vp]
     lib.mla_prefill_ragged_chunk_contiguous.restype = ctypes.c_int
     lib.mla_gather_rows.argtypes = [pt, pt, pt, vp, vp, vp, vp]
@@ -207,10 +208,11 @@ def _inputs(q, k_nope, v, k_rope_pages, page_table, q_scale, k_scale, v_scale, k
 def prefill_ragged_chunk(out, lse, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,
                          buffer_row_offsets, cache_offsets, scale, mask=MLA_MASK_CAUSAL,
                          workspace=None, q_scale=None, k_scale=None, v_scale=None, k_rope_scales=None,
-                         stream=None):
+                         stream=None, flags=0):
     """mla_prefill_ragged_chunk: one buffer row.  k_nope / v are the row's K
     buffer; buffer_row_offsets [B+1] and cache_offsets [B] are that row of the
-    plan (device int32 views of the uint32 values); lse is float32 [Tq, H]."""
+    plan (device int32 views of the uint32 values); lse is float32 [Tq, H].
+    flags=MLA_CHUNK_ACCUMULATE folds the row into out / lse."""
     lib = load()
     B = page_table.shape[0]
     fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
@@ -225,7 +227,7 @@ def prefill_ragged_chunk(out, lse, q, k_nope, v, k_rope_pages, page_table, row_o
                                         ctypes.byref(d_k), ctypes.byref(d_v), ctypes.byref(d_r),
                                         ctypes.byref(d_pt), _ptr(row_offsets), _ptr(cache_lens),
                                         _ptr(buffer_row_offsets), _ptr(cache_offsets), float(scale),
-                                        int(mask), _ptr(workspace), workspace.numel(),
+                                        int(mask), int(flags), _ptr(workspace), workspace.numel(),
                                         _stream(stream)))
     return out, lse
 
@@ -257,7 +259,7 @@ def prefill_ragged_contiguous(out, q, k_nope, v, k_rope, row_offsets, cache_lens
 def prefill_ragged_chunk_contiguous(out, lse, q, k_nope, v, k_rope, row_offsets, cache_lens,
                                     buffer_row_offsets, cache_offsets, scale, mask=MLA_MASK_CAUSAL,
                                     workspace=None, q_scale=None, k_scale=None, v_scale=None,
-                                    k_rope_scales=None, stream=None):
+                                    k_rope_scales=None, stream=None, flags=0):
     """mla_prefill_ragged_chunk_contiguous: one buffer row whose K_rope is the
     row's own [S_row, 64] tensor (row t = buffer position t)."""
     lib = load()
@@ -275,7 +277,7 @@ def prefill_ragged_chunk_contiguous(out, lse, q, k_nope, v, k_rope, row_offsets,
     _check(lib.mla_prefill_ragged_chunk_contiguous(
         ctypes.byref(d_out), ctypes.byref(d_lse), ctypes.byref(d_q), ctypes.byref(d_k), ctypes.byref(d_v),
         ctypes.byref(d_r), _ptr(row_offsets), _ptr(cache_lens), _ptr(buffer_row_offsets),
-        _ptr(cache_offsets), B, float(scale), int(mask), _ptr(workspace), workspace.numel(),
+        _ptr(cache_offsets), B, float(scale), int(mask), int(flags), _ptr(workspace), workspace.numel(),
         _stream(stream)))
     return out, lse
 
@@ -318,7 +320,7 @@ class LatentRowBuffers:
 
 def prefill_latent_row(po, pl, q, cache, page_table, row_offsets, cache_lens, bro_r, co_r, w_uk,
                        w_uv, scale, buffers, rows_in_row, mask=MLA_MASK_CAUSAL, workspace=None,
-                       status=None, kv_lora_rank=512, stream=None):
+                       status=None, kv_lora_rank=512, stream=None, flags=0):
     """One buffer row from the paged latent cache: gather its rows, up-project
     K_nope and V, then the row's attention with the gathered K_rope columns."""
     n = int(rows_in_row)
@@ -330,7 +332,7 @@ def prefill_latent_row(po, pl, q, cache, page_table, row_offsets, cache_lens, br
     up_project(v.view(n, H * 128), rows[:, :kv_lora_rank], w_uv, buffers.gemm_ws, stream)
     return prefill_ragged_chunk_contiguous(po, pl, q, kn, v, rows[:, kv_lora_rank:kv_lora_rank + 64],
                                            row_offsets, cache_lens, bro_r, co_r, scale, mask,
-                                           workspace, stream=stream)
+                                           workspace, stream=stream, flags=flags)
 
 
 def merge(out, partial_out, partial_lse, row_offsets, buffer_row_offsets, stream=None):
@@ -354,12 +356,15 @@ def chunked_scratch(num_rows, total_q, heads, device="cuda"):
 
 def prefill_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens, scale,
                     buffer_token_size, total_k, mask=MLA_MASK_CAUSAL, workspace=None, scratch=None,
-                    q_scale=None, k_scale=None, v_scale=None, k_rope_scales=None, stream=None):
+                    q_scale=None, k_scale=None, v_scale=None, k_rope_scales=None, stream=None,
+                    fold=False, lse=None):
     """Chunked execution: the plan, one mla_prefill_ragged_chunk per buffer
-    row, then mla_prefill_merge.  k_nope / v hold the contexts packed in batch
-    order (the full-context layout), so buffer row r's K buffer is rows
-    r*T .. r*T + T - 1 of them.  total_k (host int) is the number of context
-    tokens, sum of (new + cached) lengths, which fixes the row count."""
+    row, then mla_prefill_merge (or, with fold=True, every row folded into out
+    and lse in place, lse a float32 [Tq, H] tensor or allocated here).  k_nope
+    / v hold the contexts packed in batch order (the full-context layout), so
+    buffer row r's K buffer is rows r*T .. r*T + T - 1 of them.  total_k (host
+    int) is the number of context tokens, sum of (new + cached) lengths, which
+    fixes the row count."""
     T = int(buffer_token_size)
     R = max(1, -(-int(total_k) // T))
     B = page_table.shape[0]
@@ -367,11 +372,21 @@ def prefill_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, ca
     if workspace is None:
         slots = k_rope_pages.shape[0] * k_rope_pages.shape[1] if fp8 else None
         workspace = alloc_workspace(B, q.device, slots)
+    bro, co, _, _ = plan(row_offsets, cache_lens, T, R, stream=stream)
+    Sk = k_nope.shape[0]
+    if fold:
+        if lse is None:
+            lse = torch.empty((q.shape[0], q.shape[1]), dtype=torch.float32, device=q.device)
+        for r in range(R):
+            lo, hi = r * T, min((r + 1) * T, Sk)
+            prefill_ragged_chunk(out, lse, q, k_nope[lo:hi], v[lo:hi], k_rope_pages, page_table,
+                                 row_offsets, cache_lens, bro[r], co[r], scale, mask, workspace,
+                                 q_scale, k_scale, v_scale, k_rope_scales, stream,
+                                 flags=MLA_CHUNK_ACCUMULATE)
+        return out
     if scratch is None:
         scratch = chunked_scratch(R, q.shape[0], q.shape[1], q.device)
     po, pl = scratch
-    bro, co, _, _ = plan(row_offsets, cache_lens, T, R, stream=stream)
-    Sk = k_nope.shape[0]
     for r in range(R):
         lo, hi = r * T, min((r + 1) * T, Sk)
         prefill_ragged_chunk(po[r], pl[r], q, k_nope[lo:hi], v[lo:hi], k_rope_pages, page_table,

@@ -63,6 +63,8 @@ __device__ __forceinline__ uint32_t col_s(int q) { return q ? 128u : 0u; }
 __device__ __forceinline__ uint32_t col_o(int q) { return q ? 384u : 256u; }
 constexpr uint32_t kMaxBatch = 4096;
 constexpr uint64_t kL2GroupBytes = 32ull << 20;  // K/V bytes a head group should keep in L2
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
 
 // Layout and numerics that depend on the input type.
 template <bool FP8>
@@ -108,6 +110,7 @@ struct AttnParams {
   long long out_tok, out_head;
   float* lse;                 // chunked calls: [Tq, H] natural-log sum of exp(scores), else NULL
   long long lse_tok, lse_head;
+  uint32_t accumulate;        // chunked calls: fold into out / lse of the earlier rows
   const uint32_t* page_table;
   long long pt_stride;
   const uint8_t* rope_base;
@@ -849,8 +852,9 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
     const int nkv = q ? it.nkv1 : it.nkv0;
     const int i = it.i0 + q * kBM + r;  // query index inside the sequence
     if (nkv == 0) {
-      // Chunked call, no query of this tile sees a key of the window.
-      if (i < it.n) {
+      // Chunked call, no query of this tile sees a key of the window.  A
+      // folding call leaves the earlier rows' result as it is.
+      if (i < it.n && !(p.accumulate && it.co > 0)) {
         const long long row = it.q_row0 + q * kBM + r;
         uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.out_tok + static_cast<long long>(it.h) * p.out_head);
 #pragma unroll
@@ -966,25 +970,60 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
     ++of;
     tc_fence_after();
     // A row that saw no key (chunked calls only) has l = 0 and O = 0.
-    const float inv = l > 0.f ? out_scale / l : 0.f;
-    const uint64_t inv2 = f2_pack(inv, inv);
+    float inv = l > 0.f ? out_scale / l : 0.f;
     const bool store = i < it.n;
     const long long row = it.q_row0 + q * kBM + r;
     uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.out_tok + static_cast<long long>(it.h) * p.out_head);
-    if (p.lse && store)
-      p.lse[row * p.lse_tok + static_cast<long long>(it.h) * p.lse_head] =
-          l > 0.f ? (m_used + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+    // Folding chunked calls: out / lse already hold the result over the
+    // sequence's earlier buffer rows (its window does not start at context
+    // position 0); combine by log-sum-exp weights, old : new = wo : wn.
+    float keep = 0.f;  // weight of the old output row
+    if (p.lse && store) {
+      float* lp = p.lse + row * p.lse_tok + static_cast<long long>(it.h) * p.lse_head;
+      float lse = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      if (p.accumulate && it.co > 0) {
+        const float old = *lp;
+        const float mx = fmaxf(old, lse);
+        if (mx > -INFINITY) {
+          const float wo = ex2_approx((old - mx) * kLog2e), wn = ex2_approx((lse - mx) * kLog2e);
+          const float den = 1.f / (wo + wn);
+          keep = wo * den;
+          inv *= wn * den;
+          lse = mx + __log2f(wo + wn) * kLn2;
+        }
+      }
+      *lp = lse;
+    }
+    const uint64_t inv2 = f2_pack(inv, inv);
+    const uint64_t keep2 = f2_pack(keep, keep);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
       tmem_ld_32x32b_x32(t_o + 32 * c, o);
       tmem_ld_wait();
       uint32_t pk[16];
+      if (keep > 0.f) {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        float x0, x1;
-        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2), x0, x1);
-        pk[e] = pack_bf16x2(x0, x1);
+        for (int v = 0; v < 4; ++v) {
+          const uint4 w4 = dst[4 * c + v];
+          const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k = 4 * v + e;
+            const uint64_t prev = f2_pack(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), inv2,
+                             f2_mul(prev, keep2)), x0, x1);
+            pk[k] = pack_bf16x2(x0, x1);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float x0, x1;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2), x0, x1);
+          pk[e] = pack_bf16x2(x0, x1);
+        }
       }
       if (store) {
 #pragma unroll
@@ -1135,10 +1174,11 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
                      const mla_tensor_t* k_nope, const mla_tensor_t* v, const mla_tensor_t* k_rope_pages,
                      const mla_tensor_t* page_table, uint32_t contig_batch, const uint32_t* row_offsets,
                      const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
-                     const uint32_t* cache_offsets, float scale, mla_mask_t mask, void* workspace,
-                     size_t workspace_bytes, mla_stream_t stream) {
+                     const uint32_t* cache_offsets, float scale, mla_mask_t mask, uint32_t flags,
+                     void* workspace, size_t workspace_bytes, mla_stream_t stream) {
   mla_status_t st;
   const bool chunk = buffer_row_offsets != nullptr;
+  if (flags & ~MLA_CHUNK_ACCUMULATE) return fail(MLA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
   const bool contig = page_table == nullptr;
   if (!q) return fail(MLA_ERR_INVALID_ARG, "q descriptor is NULL");
   const bool fp8 = q->dtype == MLA_DTYPE_FP8_E4M3;
@@ -1288,6 +1328,7 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     prm.lse = static_cast<float*>(lse->data);
     prm.lse_tok = lse->stride[0];
     prm.lse_head = lse->stride[1];
+    prm.accumulate = (flags & MLA_CHUNK_ACCUMULATE) ? 1u : 0u;
   }
   prm.page_table = contig ? nullptr : static_cast<const uint32_t*>(page_table->data);
   prm.pt_stride = contig ? 0 : page_table->stride[0];
@@ -1339,19 +1380,20 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
                                            size_t workspace_bytes, mla_stream_t stream) {
   if (!page_table) return mla::fail(MLA_ERR_INVALID_ARG, "page_table descriptor is NULL");
   return mla::prefill(out, nullptr, q, k_nope, v, k_rope_pages, page_table, 0, row_offsets, cache_lens,
-                      nullptr, nullptr, scale, mask, workspace, workspace_bytes, stream);
+                      nullptr, nullptr, scale, mask, 0u, workspace, workspace_bytes, stream);
 }
 
 extern "C" mla_status_t mla_prefill_ragged_chunk_contiguous(
     const mla_tensor_t* out, const mla_tensor_t* lse, const mla_tensor_t* q, const mla_tensor_t* k_nope,
     const mla_tensor_t* v, const mla_tensor_t* k_rope, const uint32_t* row_offsets,
     const uint32_t* cache_lens, const uint32_t* buffer_row_offsets, const uint32_t* cache_offsets,
-    uint32_t batch, float scale, mla_mask_t mask, void* workspace, size_t workspace_bytes,
-    mla_stream_t stream) {
+    uint32_t batch, float scale, mla_mask_t mask, uint32_t flags, void* workspace,
+    size_t workspace_bytes, mla_stream_t stream) {
   if (!buffer_row_offsets) return mla::fail(MLA_ERR_INVALID_ARG, "buffer_row_offsets is NULL");
   if (batch < 1) return mla::fail(MLA_ERR_INVALID_ARG, "batch must be >= 1");
   return mla::prefill(out, lse, q, k_nope, v, k_rope, nullptr, batch, row_offsets, cache_lens,
-                      buffer_row_offsets, cache_offsets, scale, mask, workspace, workspace_bytes, stream);
+                      buffer_row_offsets, cache_offsets, scale, mask, flags, workspace, workspace_bytes,
+                      stream);
 }
 
 extern "C" mla_status_t mla_prefill_ragged_contiguous(const mla_tensor_t* out, const mla_tensor_t* q,
@@ -1363,19 +1405,20 @@ extern "C" mla_status_t mla_prefill_ragged_contiguous(const mla_tensor_t* out, c
                                                       size_t workspace_bytes, mla_stream_t stream) {
   if (batch < 1) return mla::fail(MLA_ERR_INVALID_ARG, "batch must be >= 1");
   return mla::prefill(out, nullptr, q, k_nope, v, k_rope, nullptr, batch, row_offsets, cache_lens,
-                      nullptr, nullptr, scale, mask, workspace, workspace_bytes, stream);
+                      nullptr, nullptr, scale, mask, 0u, workspace, workspace_bytes, stream);
 }
 
 extern "C" mla_status_t mla_prefill_ragged_chunk(
     const mla_tensor_t* out, const mla_tensor_t* lse, const mla_tensor_t* q, const mla_tensor_t* k_nope,
     const mla_tensor_t* v, const mla_tensor_t* k_rope_pages, const mla_tensor_t* page_table,
     const uint32_t* row_offsets, const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
-    const uint32_t* cache_offsets, float scale, mla_mask_t mask, void* workspace, size_t workspace_bytes,
-    mla_stream_t stream) {
+    const uint32_t* cache_offsets, float scale, mla_mask_t mask, uint32_t flags, void* workspace,
+    size_t workspace_bytes, mla_stream_t stream) {
   if (!buffer_row_offsets) return mla::fail(MLA_ERR_INVALID_ARG, "buffer_row_offsets is NULL");
   if (!page_table) return mla::fail(MLA_ERR_INVALID_ARG, "page_table descriptor is NULL");
   return mla::prefill(out, lse, q, k_nope, v, k_rope_pages, page_table, 0, row_offsets, cache_lens,
-                      buffer_row_offsets, cache_offsets, scale, mask, workspace, workspace_bytes, stream);
+                      buffer_row_offsets, cache_offsets, scale, mask, flags, workspace, workspace_bytes,
+                      stream);
 }
 
 // ------------------------------------------------------------ no-allocation entry point

@@ -130,15 +130,15 @@ def test_plan_rejects_bad_arguments(lib):
     assert b"buffer_token_size" in lib.mla_last_error_string() or lib.mla_last_error_string()
 
 
-def _call_chunk(lib, a, lse, bro=0x60000, co=0x70000):
+def _call_chunk(lib, a, lse, bro=0x60000, co=0x70000, flags=0):
     r = lambda d: None if d is None else ctypes.byref(d)
     return lib.mla_prefill_ragged_chunk(r(a["out"]), r(lse), r(a["q"]), r(a["k"]), r(a["v"]),
                                         r(a["rope"]), r(a["pt"]), a["ro"], a["cl"], bro, co,
-                                        a["scale"], a["mask"], a["ws"], a["ws_bytes"], None)
+                                        a["scale"], a["mask"], flags, a["ws"], a["ws_bytes"], None)
 
 
 @pytest.mark.parametrize("case", ["no_lse", "lse_shape", "lse_dtype", "lse_unaligned", "no_bro",
-                                  "no_co", "empty_row", "q_depth"])
+                                  "no_co", "empty_row", "q_depth", "flags"])
 def test_chunk_rejects_bad_arguments(lib, case):
     a = _ragged_args()
     lse = _desc([10, 2], binding.MLA_DTYPE_F32, ptr=0x80000)
@@ -159,7 +159,8 @@ def test_chunk_rejects_bad_arguments(lib, case):
         a = _ragged_args(k=_desc([0, 2, 128]), v=_desc([0, 2, 128]))
     elif case == "q_depth":
         a = _ragged_args(q=_desc([10, 2, 128]))
-    assert _call_chunk(lib, a, lse, bro, co) == binding.MLA_ERR_INVALID_ARG
+    flags = 0x6 if case == "flags" else 0
+    assert _call_chunk(lib, a, lse, bro, co, flags) == binding.MLA_ERR_INVALID_ARG
     assert lib.mla_last_error_string()
 
 

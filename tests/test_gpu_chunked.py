@@ -174,3 +174,44 @@ def test_full_size_chunked_sampled(lib, name):
     sel = ~np.isnan(ref)
     (oa, orr), _ = _tols(w)
     _close(got[sel], ref[sel], oa, orr, name)
+
+
+def _full_window(w):
+    from oracle import plan as oplan
+    bro, co, _, R = oplan.plan_formula(w.row_offsets, w.prior, max(1, w.total_k), 1)
+    assert R == 1
+    return bro[0], co[0]
+
+
+@pytest.mark.parametrize("case", ["tiny_T32", "ragged_T100_gather", "T1_one_key_rows", "page12_T37",
+                                  "null_mask_T200", "long_prior_T300", "fp8_T100"])
+def test_chunked_fold_in_place(lib, case):
+    """MLA_CHUNK_ACCUMULATE: rows folded into out / lse in row order, no merge;
+    out must be the full-context result and lse the full-context lse."""
+    from mla_ragged_paged_gb300 import binding
+    name, kw, T = CASES[case]
+    if name is not None:
+        w = workloads.generate(workloads.config(name))
+    else:
+        kw = dict(dict(heads=2, page_size=16, seed=750 + list(CASES).index(case)), **kw)
+        n, prior = kw.pop("n"), kw.pop("prior")
+        w = workloads.custom(n, prior, **kw)
+    d = workloads.device_inputs(w)
+    pool = d["k_rope_pool"][..., w.spec.rope_col:w.spec.rope_col + 64]
+    slots = w.num_pages * w.page_size if w.spec.dtype == "fp8" else None
+    ws = binding.alloc_workspace(w.batch, fp8_pool_slots=slots)
+    mask = binding.MLA_MASK_CAUSAL if w.spec.mask == "causal" else binding.MLA_MASK_NULL
+    out = torch.full((w.total_q, w.heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((w.total_q, w.heads), float("nan"), dtype=torch.float32, device="cuda")
+    binding.prefill_chunked(out, d["q"], d["k_nope"], d["v"], pool, d["page_table"], d["row_offsets"],
+                            d["cache_lens"], w.scale, T, w.total_k, mask=mask, workspace=ws,
+                            q_scale=d.get("q_scale"), k_scale=d.get("k_scale"), v_scale=d.get("v_scale"),
+                            k_rope_scales=d.get("k_rope_scales"), fold=True, lse=lse)
+    assert binding.device_status(ws) == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    got_lse = lse.cpu().numpy().astype(np.float64)
+    (oa, orr), (la, lr) = _tols(w)
+    assert np.isfinite(got).all() and np.isfinite(got_lse).all()
+    _close(got, oatt.reference(w), oa, orr, f"{case} folded out")
+    _, ref_lse = och.window_reference(w, *_full_window(w))
+    _close(got_lse, ref_lse, la, lr, f"{case} folded lse")

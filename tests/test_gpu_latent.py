@@ -87,7 +87,7 @@ def test_up_project(lib, rows, heads):
     _close(_f64(out).reshape(rows, heads, 128), ref, 1e-2, "up_project")
 
 
-def _run_latent(w, pool, w_uk, w_uv, T):
+def _run_latent(w, pool, w_uk, w_uv, T, fold=False):
     from mla_ragged_paged_gb300 import binding
     d = workloads.device_inputs(w)
     S = w.total_k
@@ -100,20 +100,28 @@ def _run_latent(w, pool, w_uk, w_uv, T):
     ws = binding.alloc_workspace(w.batch)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     mask = binding.MLA_MASK_CAUSAL if w.spec.mask == "causal" else binding.MLA_MASK_NULL
-    for r in range(R):
-        binding.prefill_latent_row(po[r], pl[r], d["q"], cache, d["page_table"], d["row_offsets"],
-                                   d["cache_lens"], bro[r], co[r], uk, uv, w.scale, bufs,
-                                   int(blen_h[r]), mask, ws, status)
-        assert binding.device_status(ws) == 0
     out = torch.full((w.total_q, w.heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
-    binding.merge(out, po, pl, d["row_offsets"], bro)
+    lse = torch.empty((w.total_q, w.heads), dtype=torch.float32, device="cuda")
+    for r in range(R):
+        if fold:
+            binding.prefill_latent_row(out, lse, d["q"], cache, d["page_table"], d["row_offsets"],
+                                       d["cache_lens"], bro[r], co[r], uk, uv, w.scale, bufs,
+                                       int(blen_h[r]), mask, ws, status, flags=binding.MLA_CHUNK_ACCUMULATE)
+        else:
+            binding.prefill_latent_row(po[r], pl[r], d["q"], cache, d["page_table"], d["row_offsets"],
+                                       d["cache_lens"], bro[r], co[r], uk, uv, w.scale, bufs,
+                                       int(blen_h[r]), mask, ws, status)
+        assert binding.device_status(ws) == 0
+    if not fold:
+        binding.merge(out, po, pl, d["row_offsets"], bro)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return _f64(out)
 
 
+@pytest.mark.parametrize("fold", [False, True])
 @pytest.mark.parametrize("case", ["small_T64", "ragged_T128", "null_T200", "page12_T37"])
-def test_latent_chunked_matches_oracle(lib, case):
+def test_latent_chunked_matches_oracle(lib, case, fold):
     cfg = {
         "small_T64": (dict(n=[150, 0, 40], prior=[70, 9, 0]), 64),
         "ragged_T128": (dict(n=[300, 17, 513], prior=[0, 700, 129], heads=4, page_size=128), 128),
@@ -122,7 +130,7 @@ def test_latent_chunked_matches_oracle(lib, case):
     }[case]
     kw, T = cfg
     w, pool, w_uk, w_uv = _setup(seed=910 + len(case), **kw)
-    got = _run_latent(w, pool, w_uk, w_uv, T)
+    got = _run_latent(w, pool, w_uk, w_uv, T, fold)
     _close(got, olat.reference(w, pool, w_uk, w_uv), 2e-2, case)
 
 
@@ -130,7 +138,7 @@ def test_latent_full_size_sampled(lib):
     """DeepSeek-V3 shapes (B=8, H=128, T=4096), sampled rows and heads."""
     w = workloads.generate(workloads.config("deepseek_v3_bf16"))
     pool, w_uk, w_uv = workloads.latent_cache(w)
-    got = _run_latent(w, pool, w_uk, w_uv, w.spec.buffer_token_size)
+    got = _run_latent(w, pool, w_uk, w_uv, w.spec.buffer_token_size, fold=True)
     assert np.isfinite(got).all()
     rng = np.random.default_rng(6)
     rows = {b: np.unique(np.concatenate([[0, int(w.n[b]) - 1], rng.integers(0, int(w.n[b]), 6)]))
