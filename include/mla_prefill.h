@@ -199,6 +199,35 @@ mla_status_t mla_prefill_ragged_contiguous(const mla_tensor_t* out, const mla_te
                                            mla_stream_t stream);
 
 /*
+ * Ragged MLA prefill attention with Q split into q_nope and q_rope
+ * (flare_mla_prefill: the overloads taking q_nope, q_rope, q_scale, k_scales;
+ * k_rope as a plain tensor, or from the paged cache).
+ *
+ * The result is that of mla_prefill_ragged with q = [q_nope | q_rope]:
+ *   q_nope   device [Tq, H, 128], bf16 or fp8 e4m3 with a per-tensor scale
+ *            (the pages' q_scale; scale_gran MLA_SCALE_PER_TENSOR)
+ *   q_rope   device bf16 [Tq, H, 64], real values (not scaled)
+ *   k_nope   device [Sk, H, 128], q_nope's dtype; fp8 with a per-tensor scale
+ *            (the pages' k_scales)
+ *   v        device [Sk, H, 128], q_nope's dtype; fp8 v without a scale of
+ *            its own is dequantised with k_nope's scale
+ *   k_rope, page_table  page_table != NULL: k_rope is the paged pool
+ *            [num_pages, P, 64] as in mla_prefill_ragged (fp8: per-token
+ *            scales); page_table == NULL: k_rope is contiguous [Sk, 64] as in
+ *            mla_prefill_ragged_contiguous
+ *   batch    B (must match page_table's rows when one is given)
+ * Workspace as for the matching fused-Q call.  Per-token (rather than
+ * per-tensor) K scales are not supported and are rejected.
+ */
+mla_status_t mla_prefill_ragged_split(const mla_tensor_t* out, const mla_tensor_t* q_nope,
+                                      const mla_tensor_t* q_rope, const mla_tensor_t* k_nope,
+                                      const mla_tensor_t* v, const mla_tensor_t* k_rope,
+                                      const mla_tensor_t* page_table, uint32_t batch,
+                                      const uint32_t* row_offsets, const uint32_t* cache_lens,
+                                      float scale, mla_mask_t mask, void* workspace,
+                                      size_t workspace_bytes, mla_stream_t stream);
+
+/*
  * mla_prefill_ragged for callers that cannot allocate device memory.  No
  * counterpart on the reference pages: it exists for callers such as a plug-in
  * whose host framework owns all device memory and offers it no scratch

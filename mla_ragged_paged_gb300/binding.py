@@ -24,6 +24,7 @@ EXPORTS = ["mla_prefill_plan", "mla_prefill_plan_max_rows", "mla_prefill_ragged_
            "mla_prefill_ragged_workspace_size_fp8", "mla_prefill_ragged", "mla_prefill_ragged_noalloc",
            "mla_prefill_ragged_chunk", "mla_prefill_merge", "mla_prefill_ragged_contiguous",
            "mla_prefill_ragged_chunk_contiguous", "mla_gather_rows", "mla_up_project",
+           "mla_prefill_ragged_split",
            "mla_read_device_status",
            "mla_last_error_string"]
 
@@ -79,6 +80,9 @@ def load(path=LIB_PATH):
                                                         ctypes.c_float, ctypes.c_int, u32, vp,
                                                         ctypes.c_size_t, vp]
     lib.mla_prefill_ragged_chunk_contiguous.restype = ctypes.c_int
+    lib.mla_prefill_ragged_split.argtypes = [pt, pt, pt, pt, pt, pt, pt, u32, vp, vp, ctypes.c_float,
+                                             ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.mla_prefill_ragged_split.restype = ctypes.c_int
     lib.mla_gather_rows.argtypes = [pt, pt, pt, vp, vp, vp, vp]
     lib.mla_gather_rows.restype = ctypes.c_int
     lib.mla_up_project.argtypes = [pt, pt, pt, vp, ctypes.c_size_t, vp]
@@ -280,6 +284,35 @@ def prefill_ragged_chunk_contiguous(out, lse, q, k_nope, v, k_rope, row_offsets,
         _ptr(cache_offsets), B, float(scale), int(mask), int(flags), _ptr(workspace), workspace.numel(),
         _stream(stream)))
     return out, lse
+
+
+def prefill_ragged_split(out, q_nope, q_rope, k_nope, v, k_rope, page_table, row_offsets, cache_lens,
+                         scale, mask=MLA_MASK_CAUSAL, workspace=None, q_scale=None, k_scale=None,
+                         v_scale=None, k_rope_scales=None, stream=None):
+    """mla_prefill_ragged_split: Q as q_nope (bf16, or fp8 with q_scale) plus a
+    bf16 q_rope; page_table None means k_rope is contiguous [Sk, 64].  fp8 v
+    without v_scale uses k_scale."""
+    lib = load()
+    B = row_offsets.numel() - 1
+    fp8 = _dtype_code(q_nope) == MLA_DTYPE_FP8_E4M3
+    if workspace is None:
+        slots = (k_rope.shape[0] * k_rope.shape[1] if page_table is not None else k_rope.shape[0]) if fp8 else None
+        workspace = alloc_workspace(B, q_nope.device, slots)
+    gran_t = MLA_SCALE_PER_TENSOR if fp8 else MLA_SCALE_NONE
+    d_out = describe(out, MLA_DTYPE_BF16)
+    d_qn = describe(q_nope, _dtype_code(q_nope), q_scale if fp8 else None, gran_t)
+    d_qr = describe(q_rope, MLA_DTYPE_BF16)
+    d_k = describe(k_nope, _dtype_code(k_nope), k_scale if fp8 else None, gran_t)
+    d_v = describe(v, _dtype_code(v), v_scale if fp8 else None, gran_t if v_scale is not None else MLA_SCALE_NONE)
+    d_r = describe(k_rope, _dtype_code(k_rope), k_rope_scales if fp8 else None,
+                   MLA_SCALE_PER_TOKEN if fp8 else MLA_SCALE_NONE)
+    d_pt = describe(page_table, MLA_DTYPE_U32) if page_table is not None else None
+    _check(lib.mla_prefill_ragged_split(ctypes.byref(d_out), ctypes.byref(d_qn), ctypes.byref(d_qr),
+                                        ctypes.byref(d_k), ctypes.byref(d_v), ctypes.byref(d_r),
+                                        ctypes.byref(d_pt) if d_pt is not None else None, B,
+                                        _ptr(row_offsets), _ptr(cache_lens), float(scale), int(mask),
+                                        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
 
 
 def gather_rows(dst, cache, page_table, buffer_row_offsets, cache_offsets, status=None, stream=None):

@@ -103,6 +103,7 @@ struct ItemInfo {
 
 struct AttnParams {
   CUtensorMap tm_q;
+  CUtensorMap tm_qr;          // split Q, bf16: q_rope [Tq, H, 64]
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_rope;
@@ -128,6 +129,10 @@ struct AttnParams {
   const float* k_scale;
   const float* v_scale;
   const float* rope_scales;  // [num_pages * page_size]
+  // Split Q (q_nope and a bf16 q_rope): q_rope rows, byte strides.
+  uint32_t q_split;
+  const uint8_t* qr_base;
+  long long qr_tok, qr_head;
 };
 
 template <bool FP8>
@@ -553,8 +558,12 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     ++q_uses[q];
     if (lane == 0) {
       mbar_arrive_expect_tx(bar, (FP8 ? 1 : 3) * kChunk);
-      for (int a = 0; a < (FP8 ? 1 : 3); ++a)
-        tma_load_3d(smem_u32(&s.q[q][a][0]), &p.tm_q, bar, 64 * a, it.h, it.q_row0 + q * kBM);
+      for (int a = 0; a < (FP8 ? 1 : 3); ++a) {
+        // Split bf16 Q: the rope atom comes from q_rope.
+        const bool rope_map = !FP8 && a == 2 && p.q_split;
+        tma_load_3d(smem_u32(&s.q[q][a][0]), rope_map ? &p.tm_qr : &p.tm_q, bar, rope_map ? 0 : 64 * a, it.h,
+                    it.q_row0 + q * kBM);
+      }
     }
     return true;
   };
@@ -642,8 +651,23 @@ __device__ __forceinline__ void load_e4m3_row(const uint8_t* src, float scale, f
   }
 }
 
+__device__ __forceinline__ void load_bf16_row(const uint8_t* src, float scale, float (&f)[64]) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 v = s4[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      f[8 * c + 2 * e] = __uint_as_float(w[e] << 16) * scale;
+      f[8 * c + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u) * scale;
+    }
+  }
+}
+
 __device__ void converter_warp(Smem<true>& s, const AttnParams& p, int lane, volatile uint32_t* abort) {
   uint32_t item_k = 0, q_uses[2] = {0, 0};
+  const float inv_sq = p.q_split ? 1.f / *p.q_scale : 1.f;
   bool alive = true;
   auto conv_q = [&](int q, const ItemInfo& it) -> bool {
     if (!mbar_wait(smem_u32(&s.q_empty[q]), (q_uses[q] & 1u) ^ 1u, abort)) return false;
@@ -652,7 +676,10 @@ __device__ void converter_warp(Smem<true>& s, const AttnParams& p, int lane, vol
     for (int r = lane; r < kBM; r += 32) {
       const int row = it.q_row0 + q * kBM + r;
       float f[64];
-      if (row < static_cast<int>(p.Tq)) {
+      if (row < static_cast<int>(p.Tq) && p.q_split) {
+        // bf16 q_rope in true units, to the units of the e4m3 codes (1 / s_q).
+        load_bf16_row(p.qr_base + row * p.qr_tok + it.h * p.qr_head, inv_sq, f);
+      } else if (row < static_cast<int>(p.Tq)) {
         load_e4m3_row(p.q_base + row * p.q_tok + it.h * p.q_head + 128, 1.f, f);
       } else {
 #pragma unroll
@@ -1170,8 +1197,9 @@ mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t*
 // chunked call (with lse).
 // page_table == NULL: K_rope is contiguous, k_rope_pages is [Sk, 64] with row
 // r holding the rope part of k_nope row r, and contig_batch gives B.
+// q_rope != NULL: split Q, q is q_nope [Tq, H, 128] and q_rope [Tq, H, 64] is bf16.
 mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla_tensor_t* q,
-                     const mla_tensor_t* k_nope, const mla_tensor_t* v, const mla_tensor_t* k_rope_pages,
+                     const mla_tensor_t* q_rope, const mla_tensor_t* k_nope, const mla_tensor_t* v, const mla_tensor_t* k_rope_pages,
                      const mla_tensor_t* page_table, uint32_t contig_batch, const uint32_t* row_offsets,
                      const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
                      const uint32_t* cache_offsets, float scale, mla_mask_t mask, uint32_t flags,
@@ -1190,12 +1218,16 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   if ((st = check_tensor(k_rope_pages, contig ? "k_rope" : "k_rope_pages", contig ? 2 : 3, dt)) != MLA_OK)
     return st;
   if (!contig && (st = check_tensor(page_table, "page_table", 2, MLA_DTYPE_U32)) != MLA_OK) return st;
+  const bool split = q_rope != nullptr;
   if (fp8) {
     const mla_tensor_t* pt[3] = {q, k_nope, v};
     const char* pn[3] = {"q", "k_nope", "v"};
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < 3; ++i) {
+      // Split Q: v without a scale of its own is dequantised with k's.
+      if (split && i == 2 && !v->scale) continue;
       if (!pt[i]->scale || pt[i]->scale_gran != MLA_SCALE_PER_TENSOR)
         return fail(MLA_ERR_INVALID_ARG, "fp8 %s needs a per-tensor scale", pn[i]);
+    }
     if (!k_rope_pages->scale || k_rope_pages->scale_gran != MLA_SCALE_PER_TOKEN)
       return fail(MLA_ERR_INVALID_ARG, "fp8 k_rope_pages needs per-token scales");
   }
@@ -1209,7 +1241,16 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   const int64_t B = contig ? static_cast<int64_t>(contig_batch) : page_table->shape[0];
   const int64_t max_pages = contig ? 0xFFFFFFFFll : page_table->shape[1];
   const int64_t NP = k_rope_pages->shape[0], P = contig ? 1 : k_rope_pages->shape[1];
-  if (q->shape[2] != 192) return fail(MLA_ERR_INVALID_ARG, "q depth must be 192");
+  if (split) {
+    if (q->shape[2] != 128) return fail(MLA_ERR_INVALID_ARG, "q_nope depth must be 128");
+    if ((st = check_tensor(q_rope, "q_rope", 3, MLA_DTYPE_BF16)) != MLA_OK) return st;
+    if (q_rope->shape[0] != Tq || q_rope->shape[1] != H || q_rope->shape[2] != 64)
+      return fail(MLA_ERR_INVALID_ARG, "q_rope must be [Tq, H, 64] matching q_nope");
+    if (!aligned16(q_rope->data) || (q_rope->stride[0] * 2) % 16 != 0 || (q_rope->stride[1] * 2) % 16 != 0)
+      return fail(MLA_ERR_INVALID_ARG, "q_rope must be 16-byte aligned with 16-byte-multiple strides");
+  } else if (q->shape[2] != 192) {
+    return fail(MLA_ERR_INVALID_ARG, "q depth must be 192");
+  }
   if (out->shape[0] != Tq || out->shape[1] != H || out->shape[2] != 128)
     return fail(MLA_ERR_INVALID_ARG, "out must be [Tq, H, 128] matching q");
   if (k_nope->shape[1] != H || k_nope->shape[2] != 128) return fail(MLA_ERR_INVALID_ARG, "k_nope must be [Sk, H, 128]");
@@ -1268,11 +1309,23 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   // Boxes are 128 bytes wide (one swizzle atom): 64 bf16 or 128 e4m3 codes.
   const uint32_t inner = fp8 ? 128 : 64;
   {
-    uint64_t dims[3] = {192, (uint64_t)H, (uint64_t)Tq};
+    uint64_t dims[3] = {split ? 128u : 192u, (uint64_t)H, (uint64_t)Tq};
     uint64_t str[2] = {(uint64_t)(q->stride[1] * es), (uint64_t)(q->stride[0] * es)};
     uint32_t box[3] = {inner, 1, kBM};
     if ((st = encode_tiled(&prm.tm_q, tdt, 3, q->data, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B, "q")) != MLA_OK)
       return st;
+    if (split) {
+      prm.q_split = 1;
+      prm.qr_base = static_cast<const uint8_t*>(q_rope->data);
+      prm.qr_tok = q_rope->stride[0] * 2;
+      prm.qr_head = q_rope->stride[1] * 2;
+      uint64_t dr[3] = {64, (uint64_t)H, (uint64_t)Tq};
+      uint64_t sr[2] = {(uint64_t)(q_rope->stride[1] * 2), (uint64_t)(q_rope->stride[0] * 2)};
+      uint32_t br[3] = {64, 1, kBM};
+      if ((st = encode_tiled(&prm.tm_qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_rope->data, dr, sr, br,
+                             CU_TENSOR_MAP_SWIZZLE_128B, "q_rope")) != MLA_OK)
+        return st;
+    }
   }
   {
     uint64_t dims[3] = {128, (uint64_t)H, (uint64_t)Sk};
@@ -1349,7 +1402,7 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   if (fp8) {
     prm.q_scale = q->scale;
     prm.k_scale = k_nope->scale;
-    prm.v_scale = v->scale;
+    prm.v_scale = v->scale ? v->scale : k_nope->scale;
     prm.rope_scales = k_rope_pages->scale;
   }
   if (fp8) {
@@ -1379,8 +1432,22 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
                                            float scale, mla_mask_t mask, void* workspace,
                                            size_t workspace_bytes, mla_stream_t stream) {
   if (!page_table) return mla::fail(MLA_ERR_INVALID_ARG, "page_table descriptor is NULL");
-  return mla::prefill(out, nullptr, q, k_nope, v, k_rope_pages, page_table, 0, row_offsets, cache_lens,
+  return mla::prefill(out, nullptr, q, nullptr, k_nope, v, k_rope_pages, page_table, 0, row_offsets, cache_lens,
                       nullptr, nullptr, scale, mask, 0u, workspace, workspace_bytes, stream);
+}
+
+extern "C" mla_status_t mla_prefill_ragged_split(
+    const mla_tensor_t* out, const mla_tensor_t* q_nope, const mla_tensor_t* q_rope, const mla_tensor_t* k_nope,
+    const mla_tensor_t* v, const mla_tensor_t* k_rope, const mla_tensor_t* page_table, uint32_t batch,
+    const uint32_t* row_offsets, const uint32_t* cache_lens, float scale, mla_mask_t mask, void* workspace,
+    size_t workspace_bytes, mla_stream_t stream) {
+  if (!q_rope) return mla::fail(MLA_ERR_INVALID_ARG, "q_rope descriptor is NULL");
+  if (batch < 1) return mla::fail(MLA_ERR_INVALID_ARG, "batch must be >= 1");
+  if (page_table && page_table->shape[0] != static_cast<int64_t>(batch))
+    return mla::fail(MLA_ERR_INVALID_ARG, "page_table has %lld rows for batch %u",
+                     (long long)page_table->shape[0], batch);
+  return mla::prefill(out, nullptr, q_nope, q_rope, k_nope, v, k_rope, page_table, batch, row_offsets,
+                      cache_lens, nullptr, nullptr, scale, mask, 0u, workspace, workspace_bytes, stream);
 }
 
 extern "C" mla_status_t mla_prefill_ragged_chunk_contiguous(
@@ -1391,7 +1458,7 @@ extern "C" mla_status_t mla_prefill_ragged_chunk_contiguous(
     size_t workspace_bytes, mla_stream_t stream) {
   if (!buffer_row_offsets) return mla::fail(MLA_ERR_INVALID_ARG, "buffer_row_offsets is NULL");
   if (batch < 1) return mla::fail(MLA_ERR_INVALID_ARG, "batch must be >= 1");
-  return mla::prefill(out, lse, q, k_nope, v, k_rope, nullptr, batch, row_offsets, cache_lens,
+  return mla::prefill(out, lse, q, nullptr, k_nope, v, k_rope, nullptr, batch, row_offsets, cache_lens,
                       buffer_row_offsets, cache_offsets, scale, mask, flags, workspace, workspace_bytes,
                       stream);
 }
@@ -1404,7 +1471,7 @@ extern "C" mla_status_t mla_prefill_ragged_contiguous(const mla_tensor_t* out, c
                                                       float scale, mla_mask_t mask, void* workspace,
                                                       size_t workspace_bytes, mla_stream_t stream) {
   if (batch < 1) return mla::fail(MLA_ERR_INVALID_ARG, "batch must be >= 1");
-  return mla::prefill(out, nullptr, q, k_nope, v, k_rope, nullptr, batch, row_offsets, cache_lens,
+  return mla::prefill(out, nullptr, q, nullptr, k_nope, v, k_rope, nullptr, batch, row_offsets, cache_lens,
                       nullptr, nullptr, scale, mask, 0u, workspace, workspace_bytes, stream);
 }
 
@@ -1416,7 +1483,7 @@ extern "C" mla_status_t mla_prefill_ragged_chunk(
     size_t workspace_bytes, mla_stream_t stream) {
   if (!buffer_row_offsets) return mla::fail(MLA_ERR_INVALID_ARG, "buffer_row_offsets is NULL");
   if (!page_table) return mla::fail(MLA_ERR_INVALID_ARG, "page_table descriptor is NULL");
-  return mla::prefill(out, lse, q, k_nope, v, k_rope_pages, page_table, 0, row_offsets, cache_lens,
+  return mla::prefill(out, lse, q, nullptr, k_nope, v, k_rope_pages, page_table, 0, row_offsets, cache_lens,
                       buffer_row_offsets, cache_offsets, scale, mask, flags, workspace, workspace_bytes,
                       stream);
 }

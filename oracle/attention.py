@@ -79,14 +79,17 @@ def attention_rows(q_rows, k_full, v, allowed, scale):
     return p @ v
 
 
-def reference(w, heads=None, rows=None, row_block=1024, out=None):
+def reference(w, heads=None, rows=None, row_block=1024, out=None, q=None):
     """Oracle output [total_q_tokens, H, 128] float64 (NaN where not computed).
 
     heads: iterable of head indices (default all).
     rows:  optional dict b -> array of local query indices; when given, only
            the sequences it names are computed (default: every row).
     out:   optional preallocated float64 [total_q_tokens, H, 128] to write the
-           computed rows into (other entries are left untouched)."""
+           computed rows into (other entries are left untouched).
+    q:     optional float64 [total_q_tokens, H, 192] query values to use
+           instead of decoding w.q (Q held in another layout, e.g. split into
+           q_nope and q_rope)."""
     fp8 = w.spec.dtype == "fp8"
     H = w.heads
     heads = list(range(H)) if heads is None else list(heads)
@@ -117,7 +120,8 @@ def reference(w, heads=None, rows=None, row_block=1024, out=None):
             v = _decode(v_raw[G:G + L, h, :], fp8, w.v_scale)
             for s0 in range(0, sel.size, row_block):
                 idx = sel[s0:s0 + row_block]
-                q_rows = _decode(q_raw[q0 + idx, h, :], fp8, w.q_scale)
+                q_rows = (q[q0 + idx, h, :] if q is not None
+                          else _decode(q_raw[q0 + idx, h, :], fp8, w.q_scale))
                 if w.spec.mask == "causal":
                     allowed = j[None, :] <= (prior + idx)[:, None]
                 else:

@@ -243,3 +243,28 @@ def test_up_project_rejects_bad_arguments(lib):
     odd = _desc([8, 512])
     odd.stride[0] = 516                                                     # 1032-byte rows
     assert f(r(out), r(odd), r(wt), None, 0, None) == bad
+
+
+@pytest.mark.parametrize("case", ["no_q_rope", "q_nope_192", "q_rope_fp8", "q_rope_shape", "batch_rows",
+                                  "batch0"])
+def test_split_rejects_bad_arguments(lib, case):
+    a = _ragged_args()
+    qn, qr, batch, pt = _desc([10, 2, 128]), _desc([10, 2, 64]), 2, a["pt"]
+    if case == "no_q_rope":
+        qr = None
+    elif case == "q_nope_192":
+        qn = _desc([10, 2, 192])
+    elif case == "q_rope_fp8":
+        qr = _desc([10, 2, 64], binding.MLA_DTYPE_FP8_E4M3)
+    elif case == "q_rope_shape":
+        qr = _desc([10, 3, 64])
+    elif case == "batch_rows":
+        batch = 3
+    elif case == "batch0":
+        batch = 0
+    r = lambda d: None if d is None else ctypes.byref(d)
+    st = lib.mla_prefill_ragged_split(r(a["out"]), r(qn), r(qr), r(a["k"]), r(a["v"]), r(a["rope"]), r(pt),
+                                      batch, a["ro"], a["cl"], a["scale"], a["mask"], a["ws"],
+                                      a["ws_bytes"], None)
+    assert st == binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_last_error_string()

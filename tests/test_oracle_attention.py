@@ -259,3 +259,11 @@ def test_generated_configs_are_finite(name):
     heads = [0, w.heads - 1]
     ref = oatt.reference(w, heads=heads)
     assert np.isfinite(ref[:, heads]).all()
+
+
+def test_explicit_query_values_replace_decoding():
+    w = workloads.custom([6, 3], [2, 5], heads=2, page_size=4, seed=31, dtype="fp8")
+    q64 = decode_e4m3(w.q.numpy()) * w.q_scale
+    np.testing.assert_array_equal(oatt.reference(w, q=q64), oatt.reference(w))
+    q64[:, :, 128:] *= 0.5                     # different rope queries change the result
+    assert not np.allclose(oatt.reference(w, q=q64), oatt.reference(w))
