@@ -252,10 +252,11 @@ def main():
     ap.add_argument("--combine", default="fold", choices=["fold", "merge"],
                     help="chunked / latent modes: fold every row into the output in place "
                          "(MLA_CHUNK_ACCUMULATE), or write per-row outputs and run mla_prefill_merge")
-    ap.add_argument("--mode", default="full", choices=["full", "chunked", "contiguous", "latent"],
+    ap.add_argument("--mode", default="full", choices=["full", "chunked", "contiguous", "latent", "split"],
                     help="full-context attention call (paged K_rope); one call per plan buffer row "
                          "plus the merge; the full-context call on a contiguous K_rope; or the "
-                         "latent-cache path (per row: gather, K/V up-projection, attention; merge)")
+                         "latent-cache path (per row: gather, K/V up-projection, attention; merge); "
+                         "or Q split into q_nope and a bf16 q_rope")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -278,6 +279,18 @@ def main():
     d = workloads.device_inputs(w, device=dev)
     contiguous = args.mode == "contiguous"
     latent = args.mode == "latent"
+    split = args.mode == "split"
+    if split:
+        # q_nope = Q[..., :128] (bf16, or the e4m3 codes); q_rope = Q[..., 128:]
+        # as bf16 real values (fp8: the rope codes times q_scale, rounded).
+        if fp8:
+            rope = w.q.view(torch.float8_e4m3fn)[..., 128:].to(torch.float32) * w.q_scale
+            d["q_rope"] = rope.to(torch.bfloat16).to(dev)
+            d["q_nope"] = w.q[..., :128].contiguous().to(dev)
+        else:
+            d["q_nope"] = w.q[..., :128].contiguous().to(dev)
+            d["q_rope"] = w.q[..., 128:].contiguous().to(dev)
+        del d["q"]
     if latent:
         assert not fp8, "the latent-cache path is bf16"
         lpool, w_uk, w_uv = workloads.latent_cache(w)
@@ -312,6 +325,12 @@ def main():
         """The attention part of a step; `tk` (a Ticker) labels its segments."""
         tick = tk.tick if tk is not None else (lambda label: None)
         tick("attn")
+        if split:
+            binding.prefill_ragged_split(o, inp["q_nope"], inp["q_rope"], inp["k_nope"], inp["v"],
+                                         inp["k_rope_pool"], inp["page_table"], inp["row_offsets"],
+                                         inp["cache_lens"], w.scale, binding.MLA_MASK_CAUSAL, ws,
+                                         stream=stream, **scales)
+            return
         if contiguous:
             binding.prefill_ragged_contiguous(o, inp["q"], inp["k_nope"], inp["v"], inp["k_rope_contig"],
                                               inp["row_offsets"], inp["cache_lens"], w.scale,
@@ -388,11 +407,14 @@ def main():
     if latent:
         for k in ("latent_pool", "w_uk", "w_uv"):
             h[k] = d[k].cpu().pin_memory()
+    if split:
+        for k in ("q_nope", "q_rope"):
+            h[k] = d[k].cpu().pin_memory()
     if contiguous:
         h["k_rope_contig"] = d["k_rope_contig"].cpu().pin_memory()
         if fp8:
             h["k_rope_scales"] = d["k_rope_scales"].cpu().pin_memory()
-    keys = ["q", "row_offsets", "cache_lens"]
+    keys = (["q_nope", "q_rope"] if split else ["q"]) + ["row_offsets", "cache_lens"]
     if latent:
         keys += ["latent_pool", "page_table", "w_uk", "w_uv"]
     else:
@@ -490,7 +512,8 @@ def main():
                                ("mla_prefill_plan + %d x mla_prefill_ragged_chunk (T=%d)%s"
                                 % (R, T, merge_txt)) if chunked else
                                ("mla_prefill_plan + mla_prefill_ragged_contiguous (K_rope [S_k, 64], not paged)"
-                                if contiguous else "mla_prefill_plan + mla_prefill_ragged")},
+                                if contiguous else "mla_prefill_plan + mla_prefill_ragged_split (q_nope + bf16 q_rope)"
+                                if split else "mla_prefill_plan + mla_prefill_ragged")},
             "pct_of_peak": 100.0 * value / world / peak,
             "clocks": clocks,
             "e2e": {"value": world * F * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
