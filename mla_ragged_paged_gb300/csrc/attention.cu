@@ -8,7 +8,7 @@
 //   P_q  = exp2(S_q * scale * log2(e) - m)   (one thread per query row)
 //   O_q += P_q . V                           (UMMA, A = P read from TMEM)
 // The two Q tiles ping-pong so one tile's softmax overlaps the other tile's
-// GEMMs.  K_rope (64 dims shared by every head) is fetched from the paged
+// GEMMs (fp8: a tile's next S is also computed while its softmax runs).  K_rope (64 dims shared by every head) is fetched from the paged
 // pool through the page table.
 //
 // Warp roles (384 threads = three warpgroups, one warp of each per SM
@@ -24,9 +24,11 @@
 // built for 168 registers per thread; warpgroup 0 then gives registers back
 // (setmaxnreg 120) so each softmax thread can hold its whole 128-column S row
 // (setmaxnreg 192): 120 + 2 * 192 = 3 * 168 per sub-partition.
-// Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,384)
-// O1 [384,512); P_q is written over the first columns of S_q (packed bf16,
-// or four e4m3 per column for fp8 inputs).
+// Tensor memory (512 columns), O0 [256,384) and O1 [384,512) in both
+// layouts.  bf16: S0 [0,128), S1 [128,256), P_q (packed bf16) written over
+// the first 64 columns of S_q.  fp8: one S region [0,128) that the score
+// tiles of Q0 and Q1 take in turn (freed as soon as the softmax has loaded
+// it), P0 [128,192) and P1 [192,256) (four e4m3 per column).
 //
 // bf16 inputs: Q0/Q1 take 3 x 16 KB each (three 64-dim 128B-swizzled K-major
 // atoms); a ring of eight 16 KB chunks carries, per KV tile, K_nope[0:64],
@@ -58,8 +60,14 @@ constexpr int kChunk = 16384;     // 128 rows x 128 bytes
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;  // registers per thread the register split assumes
 constexpr uint32_t kTmemCols = 512;
-// Tensor-memory column of S_q / O_q.
-__device__ __forceinline__ uint32_t col_s(int q) { return q ? 128u : 0u; }
+// Tensor-memory columns, O_q [256 + 128q, +128) in both layouts.  Shared S
+// region: S [0,128) for both query tiles in turn, P_q [128 + 64q, +64)
+// (four e4m3 per column).  Own regions: S_q [128q, +128), P_q over its first
+// 64 columns (packed bf16).
+__device__ __forceinline__ uint32_t col_s(bool shared, int q) { return shared ? 0u : (q ? 128u : 0u); }
+__device__ __forceinline__ uint32_t col_p(bool shared, int q) {
+  return shared ? (q ? 192u : 128u) : (q ? 128u : 0u);
+}
 __device__ __forceinline__ uint32_t col_o(int q) { return q ? 384u : 256u; }
 constexpr uint32_t kMaxBatch = 4096;
 constexpr uint64_t kL2GroupBytes = 32ull << 20;  // K/V bytes a head group should keep in L2
@@ -77,6 +85,13 @@ struct Cfg {
   static constexpr float kThreshold = FP8 ? 2.0f : 8.0f;
   // fp8: P is stored as e4m3(p * 2^6) so that P <= 2^8 stays below 448.
   static constexpr float kPScale = FP8 ? 64.0f : 1.0f;
+  // One S region shared by both query tiles plus separate P regions (the
+  // next score tile is computed during the softmax), or an S region per
+  // query tile with P written over it.  The shared region needs the K group
+  // of the next tile while V of the current one is still held; the fp8 ring
+  // (3.3 tiles) has that room, the bf16 ring (1.6 tiles) does not, and bf16
+  // measures faster with its own regions.
+  static constexpr bool kSharedS = FP8;
 };
 
 struct WsHeader {
@@ -143,6 +158,8 @@ struct __align__(1024) Smem {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[Cfg<FP8>::kRing], kv_empty[Cfg<FP8>::kRing];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t s_free[2];   // softmax q has loaded its S tile: the S region may be reused
+  uint64_t pv_done[2];  // P_q . V of the previous tile has completed: P_q and O_q are free
   uint64_t drain[2];
   ItemInfo items[2];
   uint32_t tmem_base;
@@ -726,7 +743,10 @@ __global__ void __launch_bounds__(256) rope_convert_kernel(const uint8_t* __rest
 // the other tile's UMMAs.  Both threads walk the same ring and release every
 // chunk (empty barriers count two); a thread with no work on a KV tile still
 // waits for the tile's groups before releasing them, so no barrier phase can
-// be released ahead of its fill.
+// be released ahead of its fill.  Per KV tile j a thread issues S_q(j+1) as
+// soon as the S region is free (the softmax of the score tile before it has
+// loaded it into registers) and then P_q(j) . V(j) once P_q(j) is stored, so
+// the next score tile is computed while the softmax works on this one.
 template <bool FP8>
 __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t* abort) {
   using C = Cfg<FP8>;
@@ -737,8 +757,14 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
   const uint32_t idPV = make_idesc(128, 128, 1, true);     // bf16 P.V, N = 128 over the V pair
   const uint32_t idPV8 = make_idesc(128, 128, 0, true);    // fp8 P.V, N = 128
   const uint64_t qd = sw128_desc_at(smem_u32(&s.q[q][0][0]));
-  const uint32_t d_s = tmem + col_s(q), d_o = tmem + col_o(q);
+  const uint32_t d_s = tmem + col_s(C::kSharedS, q), d_p = tmem + col_p(C::kSharedS, q);
+  const uint32_t d_o = tmem + col_o(q);
   uint32_t pos = 0, item_k = 0, qf = 0, pf = 0, oe = 0;
+  // The S region serves the score tiles in the order S0(0), S1(0), S0(1),
+  // S1(1), ... over all items.  Both issuers count them: rbase[t] = S tiles of
+  // query tile t in earlier items, rlast = query tile of the last one.
+  uint32_t rbase[2] = {0u, 0u};
+  int rlast = -1;
   bool alive = true;
 
   uint32_t fph = 0;  // full-barrier phase bit per slot, flipped at each use as a group head
@@ -778,14 +804,14 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
       const uint64_t v0 = sw128_desc_at(ring.buf(vpos));
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_f8_ts(d_o, d_s + ks * 8, v0 + ks * (4096 >> 4), idPV8, ks ? 1u : acc0);
+        umma_f8_ts(d_o, d_p + ks * 8, v0 + ks * (4096 >> 4), idPV8, ks ? 1u : acc0);
     } else {
       // 8 K-steps of 16 keys, N = 128: the two V chunks sit in adjacent slots,
       // 16 KB apart (the leading byte offset between the two 64-column atoms).
       const uint64_t v0 = sw128_desc(ring.buf(vpos), kChunk, 1024);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_f16_ts(d_o, d_s + ks * 8, v0 + ks * (2048 >> 4), idPV, ks ? 1u : acc0);
+        umma_f16_ts(d_o, d_p + ks * 8, v0 + ks * (2048 >> 4), idPV, ks ? 1u : acc0);
     }
   };
   auto release = [&](uint32_t first, int count) {
@@ -804,6 +830,14 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
   constexpr int kK = FP8 ? 2 : 3;  // K chunks per tile (ring order: K chunks, then V chunks)
   constexpr int kV = C::kCPT - kK;
 
+  // Wait until the k-th S tile of query tile t has been loaded by its softmax.
+  auto wait_region = [&](int t, uint32_t k) -> bool {
+    if (t < 0) return true;
+    if (!mbar_wait(smem_u32(&s.s_free[t]), k & 1u, abort)) return false;
+    tc_fence_after();
+    return true;
+  };
+
   while (alive) {
     const uint32_t islot = item_k & 1u;
     if (!mbar_wait(smem_u32(&s.item_full[islot]), (item_k >> 1) & 1u, abort)) break;
@@ -813,45 +847,81 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
     if (!it.valid) break;
     const int nkv = it.n1 > 0 ? it.nkv1 : it.nkv0;   // KV tiles the item streams
     if (nkv == 0) continue;                           // no query of the item sees a key
-    const int mine = q ? (it.n1 > 0 ? it.nkv1 : 0) : it.nkv0;  // tiles this query tile uses
+    const int m0 = it.nkv0, m1 = it.n1 > 0 ? it.nkv1 : 0;  // tiles of each query tile (m1 >= m0 if m1 > 0)
+    const int mine = q ? m1 : m0;
+    // Query tile t and global index k of the score tile that precedes S_q(j)
+    // in the S region.
+    auto pred = [&](int j, int& t, uint32_t& k) {
+      if (q == 0) {
+        if (j == 0) { t = rlast; k = t >= 0 ? rbase[t] - 1u : 0u; }
+        else if (j - 1 < m1) { t = 1; k = rbase[1] + j - 1; }
+        else { t = 0; k = rbase[0] + j - 1; }
+      } else {
+        if (j < m0) { t = 0; k = rbase[0] + j; }
+        else if (j == 0) { t = rlast; k = t >= 0 ? rbase[t] - 1u : 0u; }
+        else { t = 1; k = rbase[1] + j - 1; }
+      }
+    };
+    // S_q(j) into the S region once the previous score tile there has been
+    // loaded; a tile this query tile does not use only passes its K group back.
+    auto do_s = [&](int j, const TilePos& tp) -> bool {
+      if (!wait_group(tp.k)) return false;
+      if (j < mine) {
+        if (j == 0) {
+          if (!mbar_wait(smem_u32(&s.q_full[q]), qf & 1u, abort)) return false;
+          ++qf;
+          tc_fence_after();
+        }
+        if (C::kSharedS) {
+          int t;       // query tile and index of the previous S tile in the region
+          uint32_t k;
+          pred(j, t, k);
+          if (!wait_region(t, k)) return false;
+        }
+        issue_s(tp.k);
+        if (j + 1 == mine) umma_commit(smem_u32(&s.q_empty[q]));  // Q_q no longer read
+      }
+      release(tp.k, kK);
+      return true;
+    };
+    // O_q (+)= P_q(j) . V(j) once the softmax has stored P_q(j).
+    auto do_pv = [&](int j, const TilePos& tp) -> bool {
+      if (tp.pad != kNoPad) {  // pass the empty pad slot straight back
+        if (!wait_group(tp.pad)) return false;
+        release(tp.pad, 1);
+      }
+      if (!wait_group(tp.v)) return false;
+      if (j < mine) {
+        if (!wait_p(j == 0)) return false;
+        issue_pv(tp.v, j > 0);
+        if (C::kSharedS) umma_commit(smem_u32(&s.pv_done[q]));
+        if (j + 1 == mine) umma_commit(smem_u32(&s.o_full[q]));
+      }
+      release(tp.v, kV);
+      return true;
+    };
+    // Shared S region: S_q(j+1) goes ahead of P_q(j) . V(j), so the next
+    // score tile is ready when the softmax finishes this one.  Own S regions
+    // (P over S): P_q(j) . V(j) first, S_q(j+1) then overwrites P_q(j) in
+    // issue order.
     TilePos cur = tile_pos<FP8>(pos);
-    alive = wait_group(cur.k);
-    if (alive && mine > 0) {
-      alive = mbar_wait(smem_u32(&s.q_full[q]), qf & 1u, abort);
-      ++qf;
-      if (alive) {
-        tc_fence_after();
-        issue_s(cur.k);
-      }
-    }
-    if (!alive) break;
-    release(cur.k, kK);
+    alive = do_s(0, cur);
     for (int j = 0; j < nkv && alive; ++j) {
-      const bool on = j < mine;
-      const bool has_next = j + 1 < nkv;
       const TilePos nxt = tile_pos<FP8>(cur.next);
-      if (cur.pad != kNoPad) {  // pass the empty pad slot straight back
-        if (!(alive = wait_group(cur.pad))) break;
-        release(cur.pad, 1);
-      }
-      if (!(alive = wait_group(cur.v))) break;
-      if (on) {
-        if (!(alive = wait_p(j == 0))) break;
-        issue_pv(cur.v, j > 0);
-      }
-      release(cur.v, kV);
-      if (has_next) {
-        if (!(alive = wait_group(nxt.k))) break;
-        if (j + 1 < mine) issue_s(nxt.k);
-        release(nxt.k, kK);
-      }
-      if (on && j + 1 == mine) {
-        umma_commit(smem_u32(&s.o_full[q]));
-        umma_commit(smem_u32(&s.q_empty[q]));
+      if (C::kSharedS) {
+        if (j + 1 < nkv) alive = do_s(j + 1, nxt);
+        alive = alive && do_pv(j, cur);
+      } else {
+        alive = do_pv(j, cur);
+        if (alive && j + 1 < nkv) alive = do_s(j + 1, nxt);
       }
       cur = nxt;
     }
     pos = cur.k;
+    rbase[0] += static_cast<uint32_t>(m0);
+    rbase[1] += static_cast<uint32_t>(m1);
+    if (m1 > 0) rlast = 1;
+    else if (m0 > 0) rlast = 0;
   }
   // Make sure no UMMA is still in flight before tensor memory is released.
   umma_commit(smem_u32(&s.drain[q]));
@@ -864,13 +934,15 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
   using C = Cfg<FP8>;
   const int r = wq * 32 + lane;  // query row inside the tile == TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t t_s = tmem + lane_off + col_s(q);
+  const uint32_t t_s = tmem + lane_off + col_s(C::kSharedS, q);
+  const uint32_t t_p = tmem + lane_off + col_p(C::kSharedS, q);
   const uint32_t t_o = tmem + lane_off + col_o(q);
   // fp8: S in TMEM is in units of s_q * s_k; O in units of s_v * kPScale.
   const float sl2 = FP8 ? p.sl2 * (*p.q_scale) * (*p.k_scale) : p.sl2;
   const float out_scale = FP8 ? (*p.v_scale) / C::kPScale : 1.f;
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
   uint32_t item_k = 0, sf = 0, of = 0;
+  uint32_t pvc = 0;  // tiles of this query tile so far (= P.V launches that follow them)
 
   for (;;) {
     ItemInfo it;
@@ -903,6 +975,12 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(t_s + 32 * c, sr[c]);
       tmem_ld_wait();
+      if (C::kSharedS) {
+        // The S region is free for the next score tile.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.s_free[q]));
+      }
       const int key0 = j * kBN;
       const bool masked = key0 + kBN - 1 > tile_limit;
       // Columns c < nvalid are visible to this row.
@@ -955,21 +1033,28 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
             pk[e] = pack_bf16x2(p0, p1);
           }
         }
+        if (C::kSharedS && c == 0 && pvc > 0) {
+          // P_q and O_q are read / written by the previous tile's P.V until it
+          // completes.  (Own regions: S_q(j) was issued after P_q(j-1) . V, so
+          // its completion already implies that.)
+          if (!mbar_wait(smem_u32(&s.pv_done[q]), (pvc - 1) & 1u, abort)) return;
+          tc_fence_after();
+        }
         if (FP8) {
           uint32_t w8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) w8[e] = pk[e];
-          tmem_st_32x32b_x8(t_s + 8 * c, w8);
+          tmem_st_32x32b_x8(t_p + 8 * c, w8);
         } else {
-          tmem_st_32x32b_x16(t_s + 16 * c, pk);
+          tmem_st_32x32b_x16(t_p + 16 * c, pk);
         }
       }
       float l0, l1;
       f2_unpack(lacc, l0, l1);
       l += l0 + l1;
+      ++pvc;
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // The previous P.V of this tile has completed (it was issued before
-        // the S GEMM whose completion we just waited for).
+        // The previous P.V of this tile has completed (see the P stores).
         const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -1085,6 +1170,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
       mbar_init(smem_u32(&s.p_full[i]), 4);
       mbar_init(smem_u32(&s.o_full[i]), 1);
       mbar_init(smem_u32(&s.o_empty[i]), 4);
+      mbar_init(smem_u32(&s.s_free[i]), 4);   // the 4 softmax warps of query tile i
+      mbar_init(smem_u32(&s.pv_done[i]), 1);
     }
     for (int i = 0; i < C::kRing; ++i) {
       // Full barriers are per group (see producer_warp).
