@@ -8,7 +8,7 @@
 //   P_q  = exp2(S_q * scale * log2(e) - m)   (one thread per query row)
 //   O_q += P_q . V                           (UMMA, A = P read from TMEM)
 // The two Q tiles ping-pong so one tile's softmax overlaps the other tile's
-// GEMMs (fp8: a tile's next S is also computed while its softmax runs).  K_rope (64 dims shared by every head) is fetched from the paged
+// GEMMs, and a tile's next S is computed while its softmax runs.  K_rope (64 dims shared by every head) is fetched from the paged
 // pool through the page table.
 //
 // Warp roles (384 threads = three warpgroups, one warp of each per SM
@@ -24,11 +24,10 @@
 // built for 168 registers per thread; warpgroup 0 then gives registers back
 // (setmaxnreg 120) so each softmax thread can hold its whole 128-column S row
 // (setmaxnreg 192): 120 + 2 * 192 = 3 * 168 per sub-partition.
-// Tensor memory (512 columns), O0 [256,384) and O1 [384,512) in both
-// layouts.  bf16: S0 [0,128), S1 [128,256), P_q (packed bf16) written over
-// the first 64 columns of S_q.  fp8: one S region [0,128) that the score
-// tiles of Q0 and Q1 take in turn (freed as soon as the softmax has loaded
-// it), P0 [128,192) and P1 [192,256) (four e4m3 per column).
+// Tensor memory (512 columns): one S region [0,128) that the score tiles of
+// Q0 and Q1 take in turn (freed as soon as the softmax has loaded it), P0
+// [128,192) and P1 [192,256) (packed bf16, or four e4m3 per column for fp8
+// inputs), O0 [256,384), O1 [384,512).
 //
 // bf16 inputs: Q0/Q1 take 3 x 16 KB each (three 64-dim 128B-swizzled K-major
 // atoms); a ring of eight 16 KB chunks carries, per KV tile, K_nope[0:64],
@@ -60,14 +59,11 @@ constexpr int kChunk = 16384;     // 128 rows x 128 bytes
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;  // registers per thread the register split assumes
 constexpr uint32_t kTmemCols = 512;
-// Tensor-memory columns, O_q [256 + 128q, +128) in both layouts.  Shared S
-// region: S [0,128) for both query tiles in turn, P_q [128 + 64q, +64)
-// (four e4m3 per column).  Own regions: S_q [128q, +128), P_q over its first
-// 64 columns (packed bf16).
-__device__ __forceinline__ uint32_t col_s(bool shared, int q) { return shared ? 0u : (q ? 128u : 0u); }
-__device__ __forceinline__ uint32_t col_p(bool shared, int q) {
-  return shared ? (q ? 192u : 128u) : (q ? 128u : 0u);
-}
+// Tensor-memory columns: one S region [0,128) that the score tiles of both
+// query tiles take in turn, P_q [128 + 64q, +64) (packed bf16, or four e4m3
+// per column), O_q [256 + 128q, +128).
+constexpr uint32_t kColS = 0;
+__device__ __forceinline__ uint32_t col_p(int q) { return q ? 192u : 128u; }
 __device__ __forceinline__ uint32_t col_o(int q) { return q ? 384u : 256u; }
 constexpr uint32_t kMaxBatch = 4096;
 constexpr uint64_t kL2GroupBytes = 32ull << 20;  // K/V bytes a head group should keep in L2
@@ -85,13 +81,6 @@ struct Cfg {
   static constexpr float kThreshold = FP8 ? 2.0f : 8.0f;
   // fp8: P is stored as e4m3(p * 2^6) so that P <= 2^8 stays below 448.
   static constexpr float kPScale = FP8 ? 64.0f : 1.0f;
-  // One S region shared by both query tiles plus separate P regions (the
-  // next score tile is computed during the softmax), or an S region per
-  // query tile with P written over it.  The shared region needs the K group
-  // of the next tile while V of the current one is still held; the fp8 ring
-  // (3.3 tiles) has that room, the bf16 ring (1.6 tiles) does not, and bf16
-  // measures faster with its own regions.
-  static constexpr bool kSharedS = FP8;
 };
 
 struct WsHeader {
@@ -386,30 +375,26 @@ __device__ __forceinline__ Ring<Cfg<FP8>::kRing> make_ring(Smem<FP8>& s) {
 // that slot (a pad position that carries no data) so the two V chunks are
 // adjacent in shared memory and one N=128 UMMA can span them.  fp8: K_nope,
 // K_rope, V.
-struct TilePos {
-  uint32_t k, v, pad, next;  // pad == kNoPad when the tile has no pad slot
+// Ring placement of one chunk group: a K group (K_nope chunks + K_rope) or a
+// V group.  A bf16 V pair never straddles the ring end (one N = 128 UMMA
+// spans both chunks): it skips a pad slot, passed through its barriers
+// without data.  Producer and UMMA issuers place groups in the same order,
+// each K group one tile ahead of V: K(0), K(1), V(0), K(2), V(1), ... (the
+// issuers compute the next score tile before the current P.V).
+struct GroupPos {
+  uint32_t head, pad, next;  // pad == kNoPad when the group has no pad slot
 };
 constexpr uint32_t kNoPad = 0xFFFFFFFFu;
 template <bool FP8>
-__device__ __forceinline__ TilePos tile_pos(uint32_t start) {
+__device__ __forceinline__ GroupPos place_k(uint32_t pos) {
+  return {pos, kNoPad, pos + (FP8 ? 2u : 3u)};
+}
+template <bool FP8>
+__device__ __forceinline__ GroupPos place_v(uint32_t pos) {
   using C = Cfg<FP8>;
-  TilePos t;
-  t.k = start;
-  if (FP8) {
-    t.v = start + 2;
-    t.pad = kNoPad;
-    t.next = start + 3;
-  } else {
-    uint32_t v = start + 3;
-    t.pad = kNoPad;
-    if (v % C::kRing == C::kRing - 1) {
-      t.pad = v;
-      ++v;
-    }
-    t.v = v;
-    t.next = v + 2;
-  }
-  return t;
+  if (FP8) return {pos, kNoPad, pos + 1};
+  if (pos % C::kRing == C::kRing - 1) return {pos + 1, pos, pos + 3};
+  return {pos, kNoPad, pos + 2};
 }
 
 // Reads the next work item from the item ring (every consumer warp reads
@@ -605,21 +590,31 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     const bool boxes = !p.rope_contig && !p.rope_manual && it.co % static_cast<int>(p.rope_box) == 0;
     RopeFetch rf = {0u, 0u, 0u};
     if (boxes && nkv > 0) rf = rope_fetch(it, 0);
-    for (int j = 0; j < nkv && alive; ++j) {
-      const TilePos tp = tile_pos<FP8>(pos);
-      alive = load_k_group(it, j, tp.k, boxes, rf);
+    auto k_group = [&](int j) -> bool {
+      const GroupPos g = place_k<FP8>(pos);
+      pos = g.next;
+      const bool ok = load_k_group(it, j, g.head, boxes, rf);
       if (boxes && j + 1 < nkv) rf = rope_fetch(it, j + 1);
-      // A query tile that sees no key of the window is not loaded.
-      if (alive && j == 0) alive = (it.nkv0 == 0 || load_q(0, it)) && (it.nkv1 == 0 || load_q(1, it));
-      if (alive && tp.pad != kNoPad) {  // pad slot: keeps the V pair adjacent
-        alive = acquire(tp.pad);
-        if (alive) {
-          if (lane == 0) mbar_arrive(ring.full_bar(tp.pad));
-          note_head(tp.pad);
-        }
+      return ok;
+    };
+    auto v_group = [&](int j) -> bool {
+      const GroupPos g = place_v<FP8>(pos);
+      pos = g.next;
+      if (g.pad != kNoPad) {  // pad slot: keeps the V pair adjacent
+        if (!acquire(g.pad)) return false;
+        if (lane == 0) mbar_arrive(ring.full_bar(g.pad));
+        note_head(g.pad);
       }
-      alive = alive && load_v_group(it, j, tp.v);
-      pos = tp.next;
+      return load_v_group(it, j, g.head);
+    };
+    if (nkv > 0) {
+      alive = k_group(0);
+      // A query tile that sees no key of the window is not loaded.
+      if (alive) alive = (it.nkv0 == 0 || load_q(0, it)) && (it.nkv1 == 0 || load_q(1, it));
+    }
+    for (int j = 0; j < nkv && alive; ++j) {
+      if (j + 1 < nkv) alive = k_group(j + 1);
+      alive = alive && v_group(j);
     }
   }
   if (status) atomicOr(&hdr->status, status);
@@ -757,8 +752,7 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
   const uint32_t idPV = make_idesc(128, 128, 1, true);     // bf16 P.V, N = 128 over the V pair
   const uint32_t idPV8 = make_idesc(128, 128, 0, true);    // fp8 P.V, N = 128
   const uint64_t qd = sw128_desc_at(smem_u32(&s.q[q][0][0]));
-  const uint32_t d_s = tmem + col_s(C::kSharedS, q), d_p = tmem + col_p(C::kSharedS, q);
-  const uint32_t d_o = tmem + col_o(q);
+  const uint32_t d_s = tmem + kColS, d_p = tmem + col_p(q), d_o = tmem + col_o(q);
   uint32_t pos = 0, item_k = 0, qf = 0, pf = 0, oe = 0;
   // The S region serves the score tiles in the order S0(0), S1(0), S0(1),
   // S1(1), ... over all items.  Both issuers count them: rbase[t] = S tiles of
@@ -864,60 +858,51 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
     };
     // S_q(j) into the S region once the previous score tile there has been
     // loaded; a tile this query tile does not use only passes its K group back.
-    auto do_s = [&](int j, const TilePos& tp) -> bool {
-      if (!wait_group(tp.k)) return false;
+    auto do_s = [&](int j) -> bool {
+      const GroupPos g = place_k<FP8>(pos);
+      pos = g.next;
+      if (!wait_group(g.head)) return false;
       if (j < mine) {
         if (j == 0) {
           if (!mbar_wait(smem_u32(&s.q_full[q]), qf & 1u, abort)) return false;
           ++qf;
           tc_fence_after();
         }
-        if (C::kSharedS) {
-          int t;       // query tile and index of the previous S tile in the region
-          uint32_t k;
-          pred(j, t, k);
-          if (!wait_region(t, k)) return false;
-        }
-        issue_s(tp.k);
+        int t;       // query tile and index of the previous S tile in the region
+        uint32_t k;
+        pred(j, t, k);
+        if (!wait_region(t, k)) return false;
+        issue_s(g.head);
         if (j + 1 == mine) umma_commit(smem_u32(&s.q_empty[q]));  // Q_q no longer read
       }
-      release(tp.k, kK);
+      release(g.head, kK);
       return true;
     };
     // O_q (+)= P_q(j) . V(j) once the softmax has stored P_q(j).
-    auto do_pv = [&](int j, const TilePos& tp) -> bool {
-      if (tp.pad != kNoPad) {  // pass the empty pad slot straight back
-        if (!wait_group(tp.pad)) return false;
-        release(tp.pad, 1);
+    auto do_pv = [&](int j) -> bool {
+      const GroupPos g = place_v<FP8>(pos);
+      pos = g.next;
+      if (g.pad != kNoPad) {  // pass the empty pad slot straight back
+        if (!wait_group(g.pad)) return false;
+        release(g.pad, 1);
       }
-      if (!wait_group(tp.v)) return false;
+      if (!wait_group(g.head)) return false;
       if (j < mine) {
         if (!wait_p(j == 0)) return false;
-        issue_pv(tp.v, j > 0);
-        if (C::kSharedS) umma_commit(smem_u32(&s.pv_done[q]));
+        issue_pv(g.head, j > 0);
+        umma_commit(smem_u32(&s.pv_done[q]));
         if (j + 1 == mine) umma_commit(smem_u32(&s.o_full[q]));
       }
-      release(tp.v, kV);
+      release(g.head, kV);
       return true;
     };
-    // Shared S region: S_q(j+1) goes ahead of P_q(j) . V(j), so the next
-    // score tile is ready when the softmax finishes this one.  Own S regions
-    // (P over S): P_q(j) . V(j) first, S_q(j+1) then overwrites P_q(j) in
-    // issue order.
-    TilePos cur = tile_pos<FP8>(pos);
-    alive = do_s(0, cur);
+    // S_q(j+1) goes ahead of P_q(j) . V(j), so the next score tile is
+    // ready when the softmax finishes this one.
+    alive = do_s(0);
     for (int j = 0; j < nkv && alive; ++j) {
-      const TilePos nxt = tile_pos<FP8>(cur.next);
-      if (C::kSharedS) {
-        if (j + 1 < nkv) alive = do_s(j + 1, nxt);
-        alive = alive && do_pv(j, cur);
-      } else {
-        alive = do_pv(j, cur);
-        if (alive && j + 1 < nkv) alive = do_s(j + 1, nxt);
-      }
-      cur = nxt;
+      if (j + 1 < nkv) alive = do_s(j + 1);
+      alive = alive && do_pv(j);
     }
-    pos = cur.k;
     rbase[0] += static_cast<uint32_t>(m0);
     rbase[1] += static_cast<uint32_t>(m1);
     if (m1 > 0) rlast = 1;
@@ -934,8 +919,8 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
   using C = Cfg<FP8>;
   const int r = wq * 32 + lane;  // query row inside the tile == TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t t_s = tmem + lane_off + col_s(C::kSharedS, q);
-  const uint32_t t_p = tmem + lane_off + col_p(C::kSharedS, q);
+  const uint32_t t_s = tmem + lane_off + kColS;
+  const uint32_t t_p = tmem + lane_off + col_p(q);
   const uint32_t t_o = tmem + lane_off + col_o(q);
   // fp8: S in TMEM is in units of s_q * s_k; O in units of s_v * kPScale.
   const float sl2 = FP8 ? p.sl2 * (*p.q_scale) * (*p.k_scale) : p.sl2;
@@ -975,12 +960,10 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(t_s + 32 * c, sr[c]);
       tmem_ld_wait();
-      if (C::kSharedS) {
-        // The S region is free for the next score tile.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&s.s_free[q]));
-      }
+      // The S region is free for the next score tile.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s.s_free[q]));
       const int key0 = j * kBN;
       const bool masked = key0 + kBN - 1 > tile_limit;
       // Columns c < nvalid are visible to this row.
@@ -1033,10 +1016,9 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
             pk[e] = pack_bf16x2(p0, p1);
           }
         }
-        if (C::kSharedS && c == 0 && pvc > 0) {
+        if (c == 0 && pvc > 0) {
           // P_q and O_q are read / written by the previous tile's P.V until it
-          // completes.  (Own regions: S_q(j) was issued after P_q(j-1) . V, so
-          // its completion already implies that.)
+          // completes.
           if (!mbar_wait(smem_u32(&s.pv_done[q]), (pvc - 1) & 1u, abort)) return;
           tc_fence_after();
         }
