@@ -145,21 +145,28 @@ class ClockSampler:
 
 
 def dist_setup():
+    """Process group from the torchrun environment: NCCL with one GPU per rank,
+    gloo where no GPU is present (the CPU reference arm, host-side tests)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     return world, rank, local
 
 
 def dist_max(x, world):
+    """Maximum of x over the ranks (the step time of a weak-scaling run)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -168,7 +175,14 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
+
+
+def rank_spec(spec, rank):
+    """Every rank runs its own batch of the same shape (weak scaling): the
+    workload's seed is offset by the rank."""
+    return spec if rank == 0 else replace(spec, seed=spec.seed + 1000 * rank)
 
 
 _ORACLE_OUT = {}
@@ -214,6 +228,7 @@ def host_cores():
 
 
 def run_reference(args, world, rank):
+    """The CPU oracle on host cores; under torchrun only rank 0 runs it."""
     if rank != 0:
         return
     w = workloads.generate(workloads.config(args.workload))
@@ -263,6 +278,9 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
 
     import mla_ragged_paged_gb300 as pkg
@@ -274,7 +292,7 @@ def main():
 
     spec = workloads.config(args.workload)
     fp8 = spec.dtype == "fp8"
-    w = workloads.generate(spec if rank == 0 else replace(spec, seed=spec.seed + 1000 * rank))
+    w = workloads.generate(rank_spec(spec, rank))
     F = causal_flops(w)
     d = workloads.device_inputs(w, device=dev)
     contiguous = args.mode == "contiguous"
