@@ -439,28 +439,49 @@ def main():
         keys += ["k_nope", "v"] + (["k_rope_contig"] if contiguous else ["k_rope_pool", "page_table"])
     if fp8:
         keys += ["q_scale", "k_scale", "v_scale", "k_rope_scales"]
-    d2 = {k: torch.empty_like(d[k]) for k in keys}
-    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    # Two device buffer sets: step i copies its inputs in on an H2D stream,
+    # runs on the compute stream and copies its output out on a D2H stream,
+    # so the copies of steps i+1 and i-1 overlap step i.
+    sets = [{k: torch.empty_like(d[k]) for k in keys} for _ in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    hosts = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
     h2d = sum(h[k].numel() * h[k].element_size() for k in keys)
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = hosts[0].numel() * hosts[0].element_size()
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in", "done", "out")}
 
-    def e2e_step():
-        for k in keys:
-            d2[k].copy_(h[k], non_blocking=True)
-        if fp8:
-            scales.update({k: d2[k] for k in ("q_scale", "k_scale", "v_scale", "k_rope_scales")})
-        step(d2, out)
-        out_host.copy_(out, non_blocking=True)
+    def e2e_steps(n):
+        for i in range(n):
+            b = i & 1
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev["done"][b])       # step i-2 no longer reads set b
+                for k in keys:
+                    sets[b][k].copy_(h[k], non_blocking=True)
+                ev["in"][b].record(s_in)
+            stream.wait_event(ev["in"][b])
+            if i >= 2:
+                stream.wait_event(ev["out"][b])          # output of step i-2 copied out
+            if fp8:
+                scales.update({k: sets[b][k] for k in ("q_scale", "k_scale", "v_scale", "k_rope_scales")})
+            step(sets[b], outs[b])
+            ev["done"][b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["done"][b])
+                hosts[b].copy_(outs[b], non_blocking=True)
+                ev["out"][b].record(s_out)
 
-    for _ in range(2):
-        e2e_step()
+    e2e_steps(2)
+    torch.cuda.synchronize(dev)
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    e2e_steps(args.e2e_steps)
+    s_out.wait_stream(stream)
+    s_out.wait_stream(s_in)
+    e1.record(s_out)
+    torch.cuda.synchronize(dev)
     barrier(world)
     e2e_ms = dist_max(e0.elapsed_time(e1), world)
 
@@ -535,7 +556,8 @@ def main():
             "pct_of_peak": 100.0 * value / world / peak,
             "clocks": clocks,
             "e2e": {"value": world * F * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "pipelining": "two buffer sets: H2D of step i+1 and D2H of step i-1 overlap step i"},
             "gpu_launches": launches_per_step * args.steps,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
