@@ -400,6 +400,17 @@ mla_status_t mla_up_project(const mla_tensor_t* out, const mla_tensor_t* latent,
 mla_status_t mla_read_device_status(const void* workspace, uint32_t* status_out,
                                     mla_stream_t stream);
 
+/*
+ * Test hook for the timeout path (no counterpart on the pages).  While
+ * enabled (process-wide), every attention launch leaves the first K group of
+ * each CTA's first work item unloaded: the UMMA issuers' bounded wait for it
+ * runs out (after a few seconds), the kernel winds down every role, waits for
+ * its copies in flight, frees tensor memory and sets
+ * MLA_DEVICE_STATUS_TIMEOUT; the output is then incomplete.  The CUDA context
+ * stays usable.  Never enable it outside tests.
+ */
+mla_status_t mla_test_inject_stall(uint32_t enable);
+
 /* Text for the last error returned to the calling thread (never NULL). */
 const char* mla_last_error_string(void);
 

@@ -24,7 +24,7 @@ EXPORTS = ["mla_prefill_plan", "mla_prefill_plan_max_rows", "mla_prefill_ragged_
            "mla_prefill_ragged_workspace_size_fp8", "mla_prefill_ragged", "mla_prefill_ragged_noalloc",
            "mla_prefill_ragged_chunk", "mla_prefill_merge", "mla_prefill_ragged_contiguous",
            "mla_prefill_ragged_chunk_contiguous", "mla_gather_rows", "mla_up_project",
-           "mla_prefill_ragged_split",
+           "mla_prefill_ragged_split", "mla_test_inject_stall",
            "mla_read_device_status",
            "mla_last_error_string"]
 
@@ -83,6 +83,8 @@ def load(path=LIB_PATH):
     lib.mla_prefill_ragged_split.argtypes = [pt, pt, pt, pt, pt, pt, pt, u32, vp, vp, ctypes.c_float,
                                              ctypes.c_int, vp, ctypes.c_size_t, vp]
     lib.mla_prefill_ragged_split.restype = ctypes.c_int
+    lib.mla_test_inject_stall.argtypes = [u32]
+    lib.mla_test_inject_stall.restype = ctypes.c_int
     lib.mla_gather_rows.argtypes = [pt, pt, pt, vp, vp, vp, vp]
     lib.mla_gather_rows.restype = ctypes.c_int
     lib.mla_up_project.argtypes = [pt, pt, pt, vp, ctypes.c_size_t, vp]
@@ -446,6 +448,12 @@ def prefill_ragged_noalloc(out, q, k_nope, v, k_rope_pages, page_table, row_offs
                                           _ptr(row_offsets), _ptr(cache_lens), float(scale),
                                           int(mask), _stream(stream)))
     return out
+
+
+def test_inject_stall(enable):
+    """mla_test_inject_stall: make attention launches run into their wait
+    timeout (tests of the timeout path only)."""
+    _check(load().mla_test_inject_stall(1 if enable else 0))
 
 
 def device_status(workspace, stream=None):

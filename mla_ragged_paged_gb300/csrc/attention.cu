@@ -122,6 +122,9 @@ struct AttnParams {
   long long rope_tok_bytes, rope_page_bytes;
   uint32_t max_pages, num_pages, page_size, rope_box, rope_manual;
   uint32_t rope_contig;  // K_rope row = K row (no page table)
+  // Tests of the timeout path only: the producer leaves the first K group of
+  // its first work item unloaded, so the UMMA issuers' wait for it runs out.
+  uint32_t test_stall;
   uint32_t H, causal;
   float sl2;
   uint8_t* ws;
@@ -593,6 +596,7 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     auto k_group = [&](int j) -> bool {
       const GroupPos g = place_k<FP8>(pos);
       pos = g.next;
+      if (p.test_stall && item_k == 1 && j == 0) return true;  // nothing arms this group's barrier
       const bool ok = load_k_group(it, j, g.head, boxes, rf);
       if (boxes && j + 1 < nkv) rf = rope_fetch(it, j + 1);
       return ok;
@@ -1262,6 +1266,8 @@ mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t*
   return MLA_OK;
 }
 
+std::atomic<uint32_t> g_test_stall{0};
+
 // Full-context call (buffer_row_offsets == NULL) or one buffer row of a
 // chunked call (with lse).
 // page_table == NULL: K_rope is contiguous, k_rope_pages is [Sk, 64] with row
@@ -1462,6 +1468,7 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   prm.page_size = static_cast<uint32_t>(P);
   prm.H = static_cast<uint32_t>(H);
   prm.causal = mask == MLA_MASK_CAUSAL;
+  prm.test_stall = g_test_stall.load(std::memory_order_relaxed);
   prm.sl2 = scale * 1.4426950408889634f;
   prm.ws = static_cast<uint8_t*>(workspace);
   prm.q_base = static_cast<const uint8_t*>(q->data);
@@ -1503,6 +1510,11 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
   if (!page_table) return mla::fail(MLA_ERR_INVALID_ARG, "page_table descriptor is NULL");
   return mla::prefill(out, nullptr, q, nullptr, k_nope, v, k_rope_pages, page_table, 0, row_offsets, cache_lens,
                       nullptr, nullptr, scale, mask, 0u, workspace, workspace_bytes, stream);
+}
+
+extern "C" mla_status_t mla_test_inject_stall(uint32_t enable) {
+  mla::g_test_stall.store(enable ? 1u : 0u, std::memory_order_relaxed);
+  return MLA_OK;
 }
 
 extern "C" mla_status_t mla_prefill_ragged_split(
