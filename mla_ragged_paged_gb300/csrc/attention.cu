@@ -16,7 +16,7 @@
 //   warp 0      producer: work-item fetch (atomic counter), TMA loads
 //   warp 1      UMMA issuer for Q0 (one thread) and tensor-memory owner
 //   warp 2      UMMA issuer for Q1 (one thread)
-//   warp 3      fp8 inputs only: K_rope / Q_rope conversion (else idle)
+//   warp 3      fp8 inputs only: Q_rope conversion to bf16 (else idle)
 //   warps 4-7   softmax + epilogue for Q0
 //   warps 8-11  softmax + epilogue for Q1
 // A warp may only touch TMEM lanes 32*(warp%4) .. +31, so each softmax
