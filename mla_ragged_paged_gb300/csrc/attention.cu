@@ -81,6 +81,7 @@ struct Cfg {
   static constexpr float kThreshold = FP8 ? 2.0f : 8.0f;
   // fp8: P is stored as e4m3(p * 2^6) so that P <= 2^8 stays below 448.
   static constexpr float kPScale = FP8 ? 64.0f : 1.0f;
+  static constexpr float kPScaleLog2 = FP8 ? 6.0f : 0.0f;  // the prescale rides in the exponent
 };
 
 struct WsHeader {
@@ -926,9 +927,10 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
   const uint32_t t_s = tmem + lane_off + kColS;
   const uint32_t t_p = tmem + lane_off + col_p(q);
   const uint32_t t_o = tmem + lane_off + col_o(q);
-  // fp8: S in TMEM is in units of s_q * s_k; O in units of s_v * kPScale.
+  // fp8: S in TMEM is in units of s_q * s_k; P, O and the row sum l carry the
+  // kPScale prescale (folded into the exponent), so O / l needs only s_v.
   const float sl2 = FP8 ? p.sl2 * (*p.q_scale) * (*p.k_scale) : p.sl2;
-  const float out_scale = FP8 ? (*p.v_scale) / C::kPScale : 1.f;
+  const float out_scale = FP8 ? *p.v_scale : 1.f;
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
   uint32_t item_k = 0, sf = 0, of = 0;
   uint32_t pvc = 0;  // tiles of this query tile so far (= P.V launches that follow them)
@@ -995,7 +997,7 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
         l *= alpha;
       }
       const float mb = m_used == -INFINITY ? 0.f : m_used;
-      const uint64_t negm = f2_pack(-mb, -mb);
+      const uint64_t negm = f2_pack(C::kPScaleLog2 - mb, C::kPScaleLog2 - mb);
       uint64_t lacc = f2_pack(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -1014,7 +1016,7 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
           lacc = f2_add(lacc, f2_pack(p0, p1));
           if (FP8) {
             // 4 codes per column: pairs e (even) and e+1 (odd) share one word.
-            const uint32_t two = pack_e4m3x2(p0 * C::kPScale, p1 * C::kPScale);
+            const uint32_t two = pack_e4m3x2(p0, p1);
             pk[e >> 1] = (e & 1) ? (pk[e >> 1] | (two << 16)) : two;
           } else {
             pk[e] = pack_bf16x2(p0, p1);
@@ -1078,7 +1080,7 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
     float keep = 0.f;  // weight of the old output row
     if (p.lse && store) {
       float* lp = p.lse + row * p.lse_tok + static_cast<long long>(it.h) * p.lse_head;
-      float lse = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      float lse = l > 0.f ? (m_used + __log2f(l) - C::kPScaleLog2) * kLn2 : -INFINITY;
       if (p.accumulate && it.co > 0) {
         const float old = *lp;
         const float mx = fmaxf(old, lse);
