@@ -48,8 +48,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic of one attention launch per workload, from the ncu captures
 # summarised in profiles/; valid only while the kernel source is unchanged.
-ATTENTION_TRAFFIC = {"source_sha1": "87d8435d34c1509f2a46a8fadbe26c0044a4baf3",
-                     "bytes_per_launch": {"deepseek_v3_bf16": 2393945000, "fp8_e4m3": 3184557000}}
+ATTENTION_TRAFFIC = {"source_sha1": "2b9a89d02f9f3d1cd41eea86444e6c19240e7c02",
+                     "bytes_per_launch": {"deepseek_v3_bf16": 2395830000, "fp8_e4m3": 3182950000}}
 
 
 def causal_flops(w):
