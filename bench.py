@@ -519,8 +519,13 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not latent:
-        rows, nh = oracle_shape_for(w, 12.0)
+        # About 10-30 s of host work: size from a short probe, then widen the
+        # head sample once if the first run came in under 10 s.
+        rows, nh = oracle_shape_for(w, 15.0)
         f, dt, sample = oracle_sample(w, rows, list(range(nh)))
+        if dt < 10.0 and nh < w.heads:
+            nh = min(w.heads, int(nh * 15.0 / max(dt, 0.1)) + 1)
+            f, dt, sample = oracle_sample(w, rows, list(range(nh)))
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
                "sample": sample + f"; {dt:.1f} s of float64 numpy on the host"}
 
