@@ -272,6 +272,9 @@ def main():
                          "plus the merge; the full-context call on a contiguous K_rope; or the "
                          "latent-cache path (per row: gather, K/V up-projection, attention; merge); "
                          "or Q split into q_nope and a bf16 q_rope")
+    ap.add_argument("--k-scales", default="tensor", choices=["tensor", "token"],
+                    help="fp8 workloads: one K_nope scale per tensor, or one per K row (the "
+                         "workload's K_nope re-quantised row by row)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -293,6 +296,11 @@ def main():
     spec = workloads.config(args.workload)
     fp8 = spec.dtype == "fp8"
     w = workloads.generate(rank_spec(spec, rank))
+    ktok = fp8 and args.k_scales == "token"
+    if args.k_scales == "token" and not fp8:
+        ap.error("--k-scales token needs an fp8 workload")
+    if ktok:
+        w = workloads.per_token_k(w)
     F = causal_flops(w)
     d = workloads.device_inputs(w, device=dev)
     contiguous = args.mode == "contiguous"
@@ -325,8 +333,10 @@ def main():
     T = spec.buffer_token_size
     R = (w.total_k + T - 1) // T
     out = torch.empty((Tq, H, 128), dtype=torch.bfloat16, device=dev)
-    ws = binding.alloc_workspace(B, dev, fp8_pool_slots=(w.total_k if contiguous else w.num_pages * w.page_size)
-                                 if fp8 else None)
+    # fp8: converted K_rope rows per pool slot, or per K row (contiguous
+    # K_rope, per-token K scales).
+    ws = binding.alloc_workspace(B, dev, fp8_pool_slots=(w.total_k if contiguous or ktok
+                                                         else w.num_pages * w.page_size) if fp8 else None)
     scales = {k: d.get(k) for k in ("q_scale", "k_scale", "v_scale", "k_rope_scales")}
     plan_out = (torch.empty((R, B + 1), dtype=torch.int32, device=dev),
                 torch.empty((R, B), dtype=torch.int32, device=dev),
@@ -380,10 +390,12 @@ def main():
                     plan_out[0][r], plan_out[1][r], w.scale, binding.MLA_MASK_CAUSAL, ws, stream=stream,
                     flags=flags)
                 continue
+            row_scales = dict(scales, k_scale=scales["k_scale"][lo:hi]) if ktok else scales
             binding.prefill_ragged_chunk(o_r, l_r, inp["q"], inp["k_nope"][lo:hi], inp["v"][lo:hi],
                                          inp["k_rope_pool"], inp["page_table"], inp["row_offsets"],
                                          inp["cache_lens"], plan_out[0][r], plan_out[1][r], w.scale,
-                                         binding.MLA_MASK_CAUSAL, ws, stream=stream, flags=flags, **scales)
+                                         binding.MLA_MASK_CAUSAL, ws, stream=stream, flags=flags,
+                                         **row_scales)
         if not fold:
             tick("merge")
             binding.merge(o, scratch[0], scratch[1], inp["row_offsets"], plan_out[0], stream=stream)
@@ -491,7 +503,7 @@ def main():
     achieved = F / (attn_ms * 1e-3) / 1e12
     traffic = None
     if ATTENTION_TRAFFIC["source_sha1"] == source_sha1() and args.mode == "full":
-        traffic = ATTENTION_TRAFFIC["bytes_per_launch"].get(spec.name)
+        traffic = ATTENTION_TRAFFIC["bytes_per_launch"].get(spec.name + (" per-token K" if ktok else ""))
     merge_roofline = None
     if chunked and not fold:
         # Algorithmic merge bytes: per (token, head), 256 + 4 bytes read from
@@ -571,6 +583,9 @@ def main():
                          "peak_source": f"{peak_src} bf16_tflops (burst)" + (" x 2 (fp8/bf16 nominal ratio)" if fp8 else "")},
             "cpu_baseline": cpu,
         }
+        if fp8:
+            line["config"]["k_scales"] = ("one K_nope scale per K row (re-quantised per row)" if ktok
+                                          else "per-tensor K_nope scale")
         if chunked:
             line["config"]["combine"] = "in-place fold (MLA_CHUNK_ACCUMULATE)" if fold else "mla_prefill_merge"
         if merge_roofline is not None:

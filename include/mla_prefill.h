@@ -58,7 +58,8 @@ typedef enum {
 typedef enum {
   MLA_SCALE_NONE = 0,
   MLA_SCALE_PER_TENSOR = 1, /* `scale` points at one float */
-  MLA_SCALE_PER_TOKEN = 2,  /* K_rope only: one float per pool slot, index page * P + slot */
+  MLA_SCALE_PER_TOKEN = 2,  /* one float per token: K_rope pool slot (index page * P + slot),
+                               contiguous K_rope row, or fp8 K_nope row (index = K row) */
 } mla_scale_gran_t;
 
 /* A strided view of device memory.  `data` addresses element [0, 0, ...];
@@ -121,7 +122,9 @@ size_t mla_prefill_ragged_workspace_size(uint32_t batch);
 
 /* Bytes of device workspace mla_prefill_ragged needs with fp8 inputs: the bf16
  * size plus 128 bytes per K_rope pool slot (pool_slots = num_pages * P), where
- * each call first writes K_rope converted to bf16 (code * s_r[slot] / s_k). */
+ * each call first writes K_rope converted to bf16 (code * s_r[slot] / s_k).
+ * With per-token K_nope scales the converted rows sit at the K rows instead:
+ * pass the number of K rows Sk as pool_slots. */
 size_t mla_prefill_ragged_workspace_size_fp8(uint32_t batch, uint64_t pool_slots);
 
 /*
@@ -143,8 +146,10 @@ size_t mla_prefill_ragged_workspace_size_fp8(uint32_t batch, uint64_t pool_slots
  *   out          device bf16 [Tq, H, 128]                       (written)
  *   q            device [Tq, H, 192], bf16 or fp8 (per-tensor scale);
  *                dims 0..127 pair with k_nope, 128..191 with K_rope
- *   k_nope, v    device [Sk, H, 128], same dtype as q (fp8: per-tensor scale),
- *                Sk >= sum of L_b
+ *   k_nope, v    device [Sk, H, 128], same dtype as q, Sk >= sum of L_b.  fp8:
+ *                per-tensor scales, or for k_nope one float per K row
+ *                (scale_gran MLA_SCALE_PER_TOKEN, [Sk] floats, > 0): key row t
+ *                is then dequantised with k_nope->scale[t]
  *   k_rope_pages device [num_pages, P, 64]; stride[1] (token stride) may exceed
  *                64, e.g. the rope tail of a wider latent row.  bf16 with bf16
  *                q; fp8 (per-token scale) with fp8 q.
@@ -155,15 +160,18 @@ size_t mla_prefill_ragged_workspace_size_fp8(uint32_t batch, uint64_t pool_slots
  *   scale        softmax scale applied to q.k (typically 1/sqrt(192))
  *   workspace    device, >= mla_prefill_ragged_workspace_size(B) bytes for bf16
  *                inputs, >= mla_prefill_ragged_workspace_size_fp8(B, num_pages * P)
- *                for fp8 inputs; 256-byte aligned; overwritten by every call, so
- *                concurrent calls need distinct workspaces.  Its first uint32 is
- *                the device status word (0 = ok; see mla_read_device_status).
+ *                for fp8 inputs (with per-token K_nope scales: (B, Sk));
+ *                256-byte aligned; overwritten by every call, so concurrent
+ *                calls need distinct workspaces.  Its first uint32 is the
+ *                device status word (0 = ok; see mla_read_device_status).
  * Shapes, dtypes, strides, alignment and 32-bit index limits are checked on the
  * host.  Offsets and page ids live on the device: an out-of-range page id or
  * page-table column makes the kernel skip that load and set a status bit
  * (MLA_DEVICE_STATUS_*) instead of faulting.
- * Launches: a one-CTA scheduler, for fp8 inputs a K_rope conversion pass, then
- * the persistent attention kernel; no host synchronisation.
+ * Launches: a one-CTA scheduler, for fp8 inputs a K_rope conversion pass
+ * (before the scheduler, or after it with per-token K_nope scales, when it
+ * converts by K row), then the persistent attention kernel; no host
+ * synchronisation.
  */
 mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_tensor_t* q,
                                 const mla_tensor_t* k_nope, const mla_tensor_t* v,
@@ -208,16 +216,18 @@ mla_status_t mla_prefill_ragged_contiguous(const mla_tensor_t* out, const mla_te
  *            (the pages' q_scale; scale_gran MLA_SCALE_PER_TENSOR)
  *   q_rope   device bf16 [Tq, H, 64], real values (not scaled)
  *   k_nope   device [Sk, H, 128], q_nope's dtype; fp8 with a per-tensor scale
- *            (the pages' k_scales)
+ *            or one scale per K row, MLA_SCALE_PER_TOKEN, [Sk] floats > 0 (the
+ *            pages' k_scales, whose granularity the pages leave open)
  *   v        device [Sk, H, 128], q_nope's dtype; fp8 v without a scale of
- *            its own is dequantised with k_nope's scale
+ *            its own is dequantised with k_nope's scale (per-tensor k_nope
+ *            only; with per-token k_nope scales v needs its own)
  *   k_rope, page_table  page_table != NULL: k_rope is the paged pool
  *            [num_pages, P, 64] as in mla_prefill_ragged (fp8: per-token
  *            scales); page_table == NULL: k_rope is contiguous [Sk, 64] as in
  *            mla_prefill_ragged_contiguous
  *   batch    B (must match page_table's rows when one is given)
- * Workspace as for the matching fused-Q call.  Per-token (rather than
- * per-tensor) K scales are not supported and are rejected.
+ * Workspace as for the matching fused-Q call (per-token K_nope scales:
+ * mla_prefill_ragged_workspace_size_fp8(B, Sk)).
  */
 mla_status_t mla_prefill_ragged_split(const mla_tensor_t* out, const mla_tensor_t* q_nope,
                                       const mla_tensor_t* q_rope, const mla_tensor_t* k_nope,
@@ -289,6 +299,8 @@ mla_status_t mla_prefill_ragged_noalloc(const mla_tensor_t* out, const mla_tenso
  *     row's own result.
  *   lse          device float32 [Tq, H] (written), 4-byte aligned
  *   k_nope, v    device [S_row, H, 128] with S_row >= buffer_row_offsets[B] >= 1
+ *                (fp8 per-token K_nope scales: the row's own [S_row] floats, and
+ *                the workspace needs mla_prefill_ragged_workspace_size_fp8(B, S_row))
  *   buffer_row_offsets  device uint32 [B+1], non-decreasing
  *   cache_offsets       device uint32 [B]; cache_offsets[b] + W_b <= L_b
  * A window outside a sequence's context sets MLA_DEVICE_STATUS_BAD_OFFSETS

@@ -126,6 +126,25 @@ def describe(t, dtype, scale=None, scale_gran=MLA_SCALE_NONE):
     return d
 
 
+def _per_token(k_scale):
+    """An fp8 k_scale of more than one float holds one scale per K row."""
+    return k_scale is not None and k_scale.numel() > 1
+
+
+def _kdesc(k_nope, k_scale, fp8):
+    """k_nope's descriptor: fp8 scale per tensor (one float) or per K row."""
+    if not fp8:
+        return describe(k_nope, _dtype_code(k_nope))
+    gran = MLA_SCALE_PER_TOKEN if _per_token(k_scale) else MLA_SCALE_PER_TENSOR
+    return describe(k_nope, _dtype_code(k_nope), k_scale, gran)
+
+
+def _rope_rows(k_nope, k_scale, pool_slots):
+    """Rows of the converted K_rope' an fp8 workspace holds: one per pool slot,
+    or one per K row with per-token K scales."""
+    return k_nope.shape[0] if _per_token(k_scale) else pool_slots
+
+
 def _dtype_code(t):
     if t.dtype == torch.bfloat16:
         return MLA_DTYPE_BF16
@@ -183,12 +202,12 @@ def prefill_ragged(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cac
     B = page_table.shape[0]
     fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
     if workspace is None:
-        slots = k_rope_pages.shape[0] * k_rope_pages.shape[1] if fp8 else None
+        slots = _rope_rows(k_nope, k_scale, k_rope_pages.shape[0] * k_rope_pages.shape[1]) if fp8 else None
         workspace = alloc_workspace(B, q.device, slots)
     gran_t = MLA_SCALE_PER_TENSOR if fp8 else MLA_SCALE_NONE
     d_out = describe(out, MLA_DTYPE_BF16)
     d_q = describe(q, _dtype_code(q), q_scale if fp8 else None, gran_t)
-    d_k = describe(k_nope, _dtype_code(k_nope), k_scale if fp8 else None, gran_t)
+    d_k = _kdesc(k_nope, k_scale, fp8)
     d_v = describe(v, _dtype_code(v), v_scale if fp8 else None, gran_t)
     d_r = describe(k_rope_pages, _dtype_code(k_rope_pages), k_rope_scales if fp8 else None,
                    MLA_SCALE_PER_TOKEN if fp8 else MLA_SCALE_NONE)
@@ -204,7 +223,7 @@ def _inputs(q, k_nope, v, k_rope_pages, page_table, q_scale, k_scale, v_scale, k
     fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
     gran_t = MLA_SCALE_PER_TENSOR if fp8 else MLA_SCALE_NONE
     return (describe(q, _dtype_code(q), q_scale if fp8 else None, gran_t),
-            describe(k_nope, _dtype_code(k_nope), k_scale if fp8 else None, gran_t),
+            _kdesc(k_nope, k_scale, fp8),
             describe(v, _dtype_code(v), v_scale if fp8 else None, gran_t),
             describe(k_rope_pages, _dtype_code(k_rope_pages), k_rope_scales if fp8 else None,
                      MLA_SCALE_PER_TOKEN if fp8 else MLA_SCALE_NONE),
@@ -223,7 +242,7 @@ def prefill_ragged_chunk(out, lse, q, k_nope, v, k_rope_pages, page_table, row_o
     B = page_table.shape[0]
     fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
     if workspace is None:
-        slots = k_rope_pages.shape[0] * k_rope_pages.shape[1] if fp8 else None
+        slots = _rope_rows(k_nope, k_scale, k_rope_pages.shape[0] * k_rope_pages.shape[1]) if fp8 else None
         workspace = alloc_workspace(B, q.device, slots)
     d_q, d_k, d_v, d_r, d_pt = _inputs(q, k_nope, v, k_rope_pages, page_table, q_scale, k_scale,
                                        v_scale, k_rope_scales)
@@ -247,11 +266,11 @@ def prefill_ragged_contiguous(out, q, k_nope, v, k_rope, row_offsets, cache_lens
     B = row_offsets.numel() - 1
     fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
     if workspace is None:
-        workspace = alloc_workspace(B, q.device, k_rope.shape[0] if fp8 else None)
+        workspace = alloc_workspace(B, q.device, _rope_rows(k_nope, k_scale, k_rope.shape[0]) if fp8 else None)
     gran_t = MLA_SCALE_PER_TENSOR if fp8 else MLA_SCALE_NONE
     d_out = describe(out, MLA_DTYPE_BF16)
     d_q = describe(q, _dtype_code(q), q_scale if fp8 else None, gran_t)
-    d_k = describe(k_nope, _dtype_code(k_nope), k_scale if fp8 else None, gran_t)
+    d_k = _kdesc(k_nope, k_scale, fp8)
     d_v = describe(v, _dtype_code(v), v_scale if fp8 else None, gran_t)
     d_r = describe(k_rope, _dtype_code(k_rope), k_rope_scales if fp8 else None,
                    MLA_SCALE_PER_TOKEN if fp8 else MLA_SCALE_NONE)
@@ -272,11 +291,11 @@ def prefill_ragged_chunk_contiguous(out, lse, q, k_nope, v, k_rope, row_offsets,
     B = row_offsets.numel() - 1
     fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
     if workspace is None:
-        workspace = alloc_workspace(B, q.device, k_rope.shape[0] if fp8 else None)
+        workspace = alloc_workspace(B, q.device, _rope_rows(k_nope, k_scale, k_rope.shape[0]) if fp8 else None)
     gran_t = MLA_SCALE_PER_TENSOR if fp8 else MLA_SCALE_NONE
     d_out, d_lse = describe(out, MLA_DTYPE_BF16), describe(lse, MLA_DTYPE_F32)
     d_q = describe(q, _dtype_code(q), q_scale if fp8 else None, gran_t)
-    d_k = describe(k_nope, _dtype_code(k_nope), k_scale if fp8 else None, gran_t)
+    d_k = _kdesc(k_nope, k_scale, fp8)
     d_v = describe(v, _dtype_code(v), v_scale if fp8 else None, gran_t)
     d_r = describe(k_rope, _dtype_code(k_rope), k_rope_scales if fp8 else None,
                    MLA_SCALE_PER_TOKEN if fp8 else MLA_SCALE_NONE)
@@ -299,12 +318,13 @@ def prefill_ragged_split(out, q_nope, q_rope, k_nope, v, k_rope, page_table, row
     fp8 = _dtype_code(q_nope) == MLA_DTYPE_FP8_E4M3
     if workspace is None:
         slots = (k_rope.shape[0] * k_rope.shape[1] if page_table is not None else k_rope.shape[0]) if fp8 else None
+        slots = _rope_rows(k_nope, k_scale, slots) if fp8 else None
         workspace = alloc_workspace(B, q_nope.device, slots)
     gran_t = MLA_SCALE_PER_TENSOR if fp8 else MLA_SCALE_NONE
     d_out = describe(out, MLA_DTYPE_BF16)
     d_qn = describe(q_nope, _dtype_code(q_nope), q_scale if fp8 else None, gran_t)
     d_qr = describe(q_rope, MLA_DTYPE_BF16)
-    d_k = describe(k_nope, _dtype_code(k_nope), k_scale if fp8 else None, gran_t)
+    d_k = _kdesc(k_nope, k_scale, fp8)
     d_v = describe(v, _dtype_code(v), v_scale if fp8 else None, gran_t if v_scale is not None else MLA_SCALE_NONE)
     d_r = describe(k_rope, _dtype_code(k_rope), k_rope_scales if fp8 else None,
                    MLA_SCALE_PER_TOKEN if fp8 else MLA_SCALE_NONE)
@@ -406,9 +426,12 @@ def prefill_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, ca
     fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
     if workspace is None:
         slots = k_rope_pages.shape[0] * k_rope_pages.shape[1] if fp8 else None
+        slots = max(slots, min(T, k_nope.shape[0])) if _per_token(k_scale) else slots
         workspace = alloc_workspace(B, q.device, slots)
     bro, co, _, _ = plan(row_offsets, cache_lens, T, R, stream=stream)
     Sk = k_nope.shape[0]
+    # Per-token K scales follow their rows into each buffer row's slice.
+    ks = (lambda lo, hi: k_scale[lo:hi]) if _per_token(k_scale) else (lambda lo, hi: k_scale)
     if fold:
         if lse is None:
             lse = torch.empty((q.shape[0], q.shape[1]), dtype=torch.float32, device=q.device)
@@ -416,7 +439,7 @@ def prefill_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, ca
             lo, hi = r * T, min((r + 1) * T, Sk)
             prefill_ragged_chunk(out, lse, q, k_nope[lo:hi], v[lo:hi], k_rope_pages, page_table,
                                  row_offsets, cache_lens, bro[r], co[r], scale, mask, workspace,
-                                 q_scale, k_scale, v_scale, k_rope_scales, stream,
+                                 q_scale, ks(lo, hi), v_scale, k_rope_scales, stream,
                                  flags=MLA_CHUNK_ACCUMULATE)
         return out
     if scratch is None:
@@ -426,7 +449,7 @@ def prefill_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, ca
         lo, hi = r * T, min((r + 1) * T, Sk)
         prefill_ragged_chunk(po[r], pl[r], q, k_nope[lo:hi], v[lo:hi], k_rope_pages, page_table,
                              row_offsets, cache_lens, bro[r], co[r], scale, mask, workspace,
-                             q_scale, k_scale, v_scale, k_rope_scales, stream)
+                             q_scale, ks(lo, hi), v_scale, k_rope_scales, stream)
     return merge(out, po[:R], pl[:R], row_offsets, bro, stream)
 
 

@@ -137,6 +137,10 @@ struct AttnParams {
   const float* k_scale;
   const float* v_scale;
   const float* rope_scales;  // [num_pages * page_size]
+  // One K_nope scale per K row ([Sk]) instead of k_scale: the score of key
+  // row t is scaled by k_tok_scales[t] in the softmax, and K_rope' (divided by
+  // the same scale) is read contiguously at the K row.
+  const float* k_tok_scales;
   // Split Q (q_nope and a bf16 q_rope): q_rope rows, byte strides.
   uint32_t q_split;
   const uint8_t* qr_base;
@@ -154,10 +158,19 @@ struct __align__(1024) Smem {
   uint64_t s_free[2];   // softmax q has loaded its S tile: the S region may be reused
   uint64_t pv_done[2];  // P_q . V of the previous tile has completed: P_q and O_q are free
   uint64_t drain[2];
+  // Per-token K scales: the 128 scales of the KV tile each softmax warpgroup
+  // is working on (filled by its threads, one key each), with barriers that
+  // count the group's four warps: written, and no longer read.
+  uint64_t ks_full[2], ks_free[2];
+  alignas(16) float ksc[2][kBN];
   ItemInfo items[2];
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
+// One CTA per SM: the struct, plus up to 1 KB to align it, within the 227 KB
+// a CTA may use.
+static_assert(sizeof(Smem<false>) + 1024 <= 232448, "shared memory (bf16)");
+static_assert(sizeof(Smem<true>) + 1024 <= 232448, "shared memory (fp8)");
 
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
@@ -738,6 +751,66 @@ __global__ void __launch_bounds__(256) rope_convert_kernel(const uint8_t* __rest
   }
 }
 
+// fp8 inputs with one K_nope scale per K row: K_rope' = e4m3 code * s_r[slot]
+// / s_k[row] for every key row of every sequence's window, written at the K
+// row (a contiguous [Sk, 64] bf16 copy, so the attention kernel reads it like
+// a contiguous K_rope).  It runs after the scheduler: the records give each
+// window's K rows, its context offset and its sequence.  Block (x, y) takes
+// records x, x + gridDim.x, ... and, inside each, every gridDim.y-th group of
+// blockDim.x keys.
+struct RopeRows {
+  const uint8_t* pool;            // e4m3 K_rope rows
+  long long tok_bytes, page_bytes;
+  const uint32_t* page_table;     // NULL: contiguous K_rope, row = K row
+  long long pt_stride;
+  uint32_t P, num_pages, max_pages, Sk;
+  const float* rope_scales;       // [num_pages * P] (contiguous: [Sk])
+  const float* k_scales;          // [Sk]
+  uint16_t* out;                  // [Sk, 64] bf16
+  uint8_t* ws;
+};
+
+__global__ void __launch_bounds__(256) rope_convert_rows_kernel(const __grid_constant__ RopeRows a) {
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
+  const SeqRec* recs = reinterpret_cast<const SeqRec*>(a.ws + sizeof(WsHeader));
+  const uint32_t nseq = hdr->num_seqs;
+  uint32_t bad = 0;
+  for (uint32_t si = blockIdx.x; si < nseq; si += gridDim.x) {
+    const SeqRec rec = recs[si];
+    const uint32_t b = rec.bg & 0xFFFFu;
+    for (uint32_t j = blockIdx.y * blockDim.x + threadIdx.x; j < rec.W; j += gridDim.y * blockDim.x) {
+      const uint32_t row = rec.kv_start + j;
+      if (row >= a.Sk) break;
+      uint32_t page = row, prow = 0;  // contiguous: a one-row page per K row
+      if (a.page_table) {
+        const uint32_t pos = rec.co + j;  // context position of the key
+        const uint32_t col = pos / a.P;
+        uint32_t pg = 0xFFFFFFFFu;
+        if (col < a.max_pages) pg = a.page_table[static_cast<long long>(b) * a.pt_stride + col];
+        else bad |= MLA_DEVICE_STATUS_BAD_COLUMN;
+        if (pg >= a.num_pages) {
+          if (col < a.max_pages) bad |= MLA_DEVICE_STATUS_BAD_PAGE;
+          uint4* dst = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(row) * 64);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+          continue;
+        }
+        page = pg;
+        prow = pos - col * a.P;
+      }
+      const long long slot = static_cast<long long>(page) * a.P + prow;
+      float f[64];
+      load_e4m3_row(a.pool + page * a.page_bytes + prow * a.tok_bytes, a.rope_scales[slot] / a.k_scales[row], f);
+      uint4* dst = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(row) * 64);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        dst[c] = make_uint4(pack_bf16x2(f[8 * c], f[8 * c + 1]), pack_bf16x2(f[8 * c + 2], f[8 * c + 3]),
+                            pack_bf16x2(f[8 * c + 4], f[8 * c + 5]), pack_bf16x2(f[8 * c + 6], f[8 * c + 7]));
+    }
+  }
+  if (bad) atomicOr(&hdr->status, bad);
+}
+
 // UMMA issue for one query tile.  Warps 1 and 2 each run this for their own
 // tile (q = 0, 1): a thread blocked on a barrier wait then no longer holds up
 // the other tile's UMMAs.  Both threads walk the same ring and release every
@@ -918,7 +991,7 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
   wait_drain(smem_u32(&s.drain[q]), 0);
 }
 
-template <bool FP8>
+template <bool FP8, bool KTOK>
 __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, int q, int wq,
                              int lane, volatile uint32_t* abort) {
   using C = Cfg<FP8>;
@@ -927,13 +1000,22 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
   const uint32_t t_s = tmem + lane_off + kColS;
   const uint32_t t_p = tmem + lane_off + col_p(q);
   const uint32_t t_o = tmem + lane_off + col_o(q);
-  // fp8: S in TMEM is in units of s_q * s_k; P, O and the row sum l carry the
-  // kPScale prescale (folded into the exponent), so O / l needs only s_v.
-  const float sl2 = FP8 ? p.sl2 * (*p.q_scale) * (*p.k_scale) : p.sl2;
+  // fp8: S in TMEM is in units of s_q * s_k (per-token K scales: s_q * s_k[key],
+  // the key's factor applied per column below); P, O and the row sum l carry
+  // the kPScale prescale (folded into the exponent), so O / l needs only s_v.
+  const float sl2 = FP8 ? p.sl2 * (*p.q_scale) * (KTOK ? 1.f : *p.k_scale) : p.sl2;
   const float out_scale = FP8 ? *p.v_scale : 1.f;
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
   uint32_t item_k = 0, sf = 0, of = 0;
   uint32_t pvc = 0;  // tiles of this query tile so far (= P.V launches that follow them)
+  uint32_t kt = 0;   // KV tiles whose key scales this warpgroup has staged
+  const uint32_t ks_full = smem_u32(&s.ks_full[q]), ks_free = smem_u32(&s.ks_free[q]);
+  const uint32_t ks_row = smem_u32(&s.ksc[q][0]);
+  // Scale of window key j * kBN + r (1 past the window: those keys are masked).
+  auto key_scale = [&](const ItemInfo& it, int j) -> float {
+    const int key = j * kBN + r;
+    return key < it.W ? __ldg(p.k_tok_scales + it.kv_row0 + key) : 1.f;
+  };
 
   for (;;) {
     ItemInfo it;
@@ -957,8 +1039,20 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
     const int limit = p.causal ? min(it.shift + i, last_key) : last_key;
     const int tile_limit = p.causal ? min(it.shift + it.i0 + q * kBM, last_key) : last_key;
     float m_used = -INFINITY, l = 0.f;
+    float ks_next = KTOK ? key_scale(it, 0) : 1.f;  // this thread's key scale for the next tile
 
     for (int j = 0; j < nkv; ++j) {
+      if (KTOK) {
+        // Stage tile j's 128 key scales (thread r holds key r's) once every
+        // warp of the group has finished reading tile j-1's; the load for
+        // tile j+1 is issued here and consumed a tile later.
+        if (kt > 0 && !mbar_wait(ks_free, (kt - 1) & 1u, abort)) return;
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(ks_row + 4u * r), "f"(ks_next) : "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ks_full);
+        if (!mbar_wait(ks_full, kt & 1u, abort)) return;
+        if (j + 1 < nkv) ks_next = key_scale(it, j + 1);
+      }
       if (!mbar_wait(smem_u32(&s.s_full[q]), sf & 1u, abort)) return;
       ++sf;
       tc_fence_after();
@@ -970,6 +1064,31 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s.s_free[q]));
+      if (KTOK) {
+        // Column c of S times its key's scale (a broadcast read: every lane
+        // reads the same four scales).
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            float k0, k1, k2, k3;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(k0), "=f"(k1), "=f"(k2), "=f"(k3)
+                         : "r"(ks_row + 4u * (32 * c + 4 * k)));
+            float x0, x1, x2, x3;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[c][4 * k]), __uint_as_float(sr[c][4 * k + 1])),
+                             f2_pack(k0, k1)), x0, x1);
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[c][4 * k + 2]), __uint_as_float(sr[c][4 * k + 3])),
+                             f2_pack(k2, k3)), x2, x3);
+            sr[c][4 * k] = __float_as_uint(x0);
+            sr[c][4 * k + 1] = __float_as_uint(x1);
+            sr[c][4 * k + 2] = __float_as_uint(x2);
+            sr[c][4 * k + 3] = __float_as_uint(x3);
+          }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ks_free);
+        ++kt;
+      }
       const int key0 = j * kBN;
       const bool masked = key0 + kBN - 1 > tile_limit;
       // Columns c < nvalid are visible to this row.
@@ -1137,7 +1256,7 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
   }
 }
 
-template <bool FP8>
+template <bool FP8, bool KTOK>
 __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<FP8>;
   extern __shared__ uint8_t smem_raw[];
@@ -1160,6 +1279,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
       mbar_init(smem_u32(&s.o_empty[i]), 4);
       mbar_init(smem_u32(&s.s_free[i]), 4);   // the 4 softmax warps of query tile i
       mbar_init(smem_u32(&s.pv_done[i]), 1);
+      mbar_init(smem_u32(&s.ks_full[i]), 4);
+      mbar_init(smem_u32(&s.ks_free[i]), 4);
     }
     for (int i = 0; i < C::kRing; ++i) {
       // Full barriers are per group (see producer_warp).
@@ -1198,7 +1319,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
-    softmax_warp<FP8>(s, p, tmem, (warp - 4) >> 2, warp & 3, lane, abort);
+    softmax_warp<FP8, KTOK>(s, p, tmem, (warp - 4) >> 2, warp & 3, lane, abort);
   }
 
   tc_fence_before();
@@ -1227,15 +1348,16 @@ extern "C" size_t mla_prefill_ragged_workspace_size_fp8(uint32_t batch, uint64_t
 namespace mla {
 namespace {
 
-// Launches the scheduler and the attention kernel for one input type.
-template <bool FP8>
+// Launches the scheduler, the per-row K_rope conversion (per-token K scales
+// only, rows != NULL) and the attention kernel for one input type.
+template <bool FP8, bool KTOK>
 mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t* row_offsets,
                               const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
                               const uint32_t* cache_offsets, uint32_t B, uint32_t H, uint32_t Tq,
                               uint32_t Sk, uint32_t P, uint32_t max_pages, void* workspace,
-                              cudaStream_t cs) {
+                              const RopeRows* rows, cudaStream_t cs) {
   mla_status_t st;
-  auto* kernel = mla_attention_kernel<FP8>;
+  auto* kernel = mla_attention_kernel<FP8, KTOK>;
   {
     // The register split inside the kernel is only safe when the kernel was
     // built with exactly kLaunchRegs registers per thread.
@@ -1254,7 +1376,9 @@ mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t*
   if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(schedule_kernel), sched_smem, dev, 1)) != MLA_OK)
     return st;
   const int attn_smem = static_cast<int>(sizeof(Smem<FP8>) + 1024);
-  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), attn_smem, dev, FP8 ? 3 : 2)) != MLA_OK)
+  // One attribute cache slot per kernel instantiation.
+  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), attn_smem, dev,
+                                 FP8 ? (KTOK ? 4 : 3) : 2)) != MLA_OK)
     return st;
   const uint32_t elt = FP8 ? 1u : 2u;
   schedule_kernel<<<1, kSchedThreads, sched_smem, cs>>>(row_offsets, cache_lens, buffer_row_offsets,
@@ -1262,6 +1386,14 @@ mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t*
                                                         elt * (128 + 128), static_cast<uint8_t*>(workspace));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "scheduler launch: %s", cudaGetErrorString(e));
+  if (rows) {
+    // About 4 blocks per SM in all, at least one per sequence record.
+    const uint32_t gy = std::max<uint32_t>(
+        1u, std::min<uint32_t>((Sk + 255) / 256, (4u * static_cast<uint32_t>(sms) + B - 1) / B));
+    rope_convert_rows_kernel<<<dim3(B, gy), 256, 0, cs>>>(*rows);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "rope conversion launch: %s", cudaGetErrorString(e));
+  }
   kernel<<<sms, kThreads, attn_smem, cs>>>(prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
@@ -1296,14 +1428,19 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     return st;
   if (!contig && (st = check_tensor(page_table, "page_table", 2, MLA_DTYPE_U32)) != MLA_OK) return st;
   const bool split = q_rope != nullptr;
+  // fp8 K_nope may carry one scale per K row instead of one per tensor.
+  const bool ktok = fp8 && k_nope->scale && k_nope->scale_gran == MLA_SCALE_PER_TOKEN;
   if (fp8) {
     const mla_tensor_t* pt[3] = {q, k_nope, v};
     const char* pn[3] = {"q", "k_nope", "v"};
     for (int i = 0; i < 3; ++i) {
-      // Split Q: v without a scale of its own is dequantised with k's.
-      if (split && i == 2 && !v->scale) continue;
+      if (i == 1 && ktok) continue;
+      // Split Q: v without a scale of its own is dequantised with k's
+      // (per-tensor k only).
+      if (split && i == 2 && !v->scale && !ktok) continue;
       if (!pt[i]->scale || pt[i]->scale_gran != MLA_SCALE_PER_TENSOR)
-        return fail(MLA_ERR_INVALID_ARG, "fp8 %s needs a per-tensor scale", pn[i]);
+        return fail(MLA_ERR_INVALID_ARG, "fp8 %s needs a per-tensor scale%s", pn[i],
+                    i == 1 ? " or one scale per row" : "");
     }
     if (!k_rope_pages->scale || k_rope_pages->scale_gran != MLA_SCALE_PER_TOKEN)
       return fail(MLA_ERR_INVALID_ARG, "fp8 k_rope_pages needs per-token scales");
@@ -1354,8 +1491,10 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     return fail(MLA_ERR_INVALID_ARG, "too many work items (query blocks x heads exceeds 2^31)");
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return fail(MLA_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
-  const size_t ws_need = fp8 ? mla_prefill_ragged_workspace_size_fp8(static_cast<uint32_t>(B),
-                                                                      static_cast<uint64_t>(NP * P))
+  // fp8: the bf16 K_rope' copy has one row per pool slot, or per K row when
+  // K scales are per token.
+  const size_t ws_need = fp8 ? mla_prefill_ragged_workspace_size_fp8(
+                                   static_cast<uint32_t>(B), static_cast<uint64_t>(ktok ? Sk : NP * P))
                              : mla_prefill_ragged_workspace_size(static_cast<uint32_t>(B));
   if (workspace_bytes < ws_need)
     return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes needed", ws_need);
@@ -1421,9 +1560,12 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     while (b) { uint32_t t = a % b; a = b; b = t; }
     g = a;  // gcd(P, 128): rows per page segment inside a key tile
   }
-  prm.rope_contig = contig;
-  prm.rope_manual = !contig && (g % 8u) != 0;
-  prm.rope_box = contig ? kBN : g;
+  // Per-token K scales: the converted K_rope' sits at the K rows, so the
+  // kernel reads it like a contiguous K_rope whatever the caller's layout.
+  const bool rows_contig = contig || ktok;
+  prm.rope_contig = rows_contig;
+  prm.rope_manual = !rows_contig && (g % 8u) != 0;
+  prm.rope_box = rows_contig ? kBN : g;
   // bf16 K_rope rows: the caller's pool, or for fp8 inputs the converted copy
   // the pre-pass writes after the scheduler records in the workspace.
   const int64_t rope_tok_el = contig ? k_rope_pages->stride[0] : k_rope_pages->stride[1];
@@ -1435,9 +1577,9 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     rope_tok = 128;
     rope_page = static_cast<uint64_t>(P) * 128;
   }
-  if (contig) {
+  if (rows_contig) {
     // One 128-row box per KV tile, at the tile's K row.
-    uint64_t dims[2] = {64, (uint64_t)NP};
+    uint64_t dims[2] = {64, (uint64_t)(ktok ? Sk : NP)};
     uint64_t str[1] = {rope_tok};
     uint32_t box[2] = {64, kBN};
     if ((st = encode_tiled(&prm.tm_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rope_rows, dims, str, box,
@@ -1479,9 +1621,31 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   prm.Tq = static_cast<uint32_t>(Tq);
   if (fp8) {
     prm.q_scale = q->scale;
-    prm.k_scale = k_nope->scale;
+    prm.k_scale = ktok ? nullptr : k_nope->scale;
+    prm.k_tok_scales = ktok ? k_nope->scale : nullptr;
     prm.v_scale = v->scale ? v->scale : k_nope->scale;
     prm.rope_scales = k_rope_pages->scale;
+  }
+  const uint32_t uB = static_cast<uint32_t>(B), uH = static_cast<uint32_t>(H), uTq = static_cast<uint32_t>(Tq),
+                 uSk = static_cast<uint32_t>(Sk), uP = static_cast<uint32_t>(P),
+                 uMP = static_cast<uint32_t>(max_pages);
+  if (ktok) {
+    RopeRows rr;
+    rr.pool = static_cast<const uint8_t*>(k_rope_pages->data);
+    rr.tok_bytes = rope_tok_el;
+    rr.page_bytes = k_rope_pages->stride[0];
+    rr.page_table = contig ? nullptr : static_cast<const uint32_t*>(page_table->data);
+    rr.pt_stride = contig ? 0 : page_table->stride[0];
+    rr.P = uP;
+    rr.num_pages = static_cast<uint32_t>(NP);
+    rr.max_pages = uMP;
+    rr.Sk = uSk;
+    rr.rope_scales = k_rope_pages->scale;
+    rr.k_scales = k_nope->scale;
+    rr.out = static_cast<uint16_t*>(rope_rows);
+    rr.ws = static_cast<uint8_t*>(workspace);
+    return launch_attention<true, true>(prm, dev, sms, row_offsets, cache_lens, buffer_row_offsets,
+                                        cache_offsets, uB, uH, uTq, uSk, uP, uMP, workspace, &rr, cs);
   }
   if (fp8) {
     const uint32_t slots = static_cast<uint32_t>(NP * P);
@@ -1492,11 +1656,9 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "rope conversion launch: %s", cudaGetErrorString(e));
   }
-  auto launch = fp8 ? launch_attention<true> : launch_attention<false>;
-  return launch(prm, dev, sms, row_offsets, cache_lens, buffer_row_offsets, cache_offsets,
-                static_cast<uint32_t>(B), static_cast<uint32_t>(H), static_cast<uint32_t>(Tq),
-                static_cast<uint32_t>(Sk), static_cast<uint32_t>(P), static_cast<uint32_t>(max_pages),
-                workspace, cs);
+  auto launch = fp8 ? launch_attention<true, false> : launch_attention<false, false>;
+  return launch(prm, dev, sms, row_offsets, cache_lens, buffer_row_offsets, cache_offsets, uB, uH, uTq, uSk,
+                uP, uMP, workspace, nullptr, cs);
 }
 
 }  // namespace

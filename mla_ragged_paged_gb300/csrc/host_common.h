@@ -31,7 +31,9 @@ bool aligned16(const void* ptr);
 // non-negative strides, innermost stride 1.
 mla_status_t check_tensor(const mla_tensor_t* t, const char* name, int ndim, mla_dtype_t dtype);
 
-// Allow `bytes` of dynamic shared memory for `func` on `device` (cached).
+// Allow `bytes` of dynamic shared memory for `func` on `device`, cached per
+// (device, slot): each kernel needs a slot of its own, 0..7 (0 plan,
+// 1 scheduler, 2 / 3 / 4 attention bf16 / fp8 / fp8 with per-token K scales).
 mla_status_t set_max_dynamic_smem(const void* func, int bytes, int device, int slot);
 
 }  // namespace mla

@@ -12,7 +12,9 @@ What is computed, per the flare_mla_prefill page:
   page, Args: mask_functor), softmax over keys, times V; the output is 128
   wide (description: "output has reduced dimension").
 * fp8 inputs are dequantised as code value times scale, K_rope with one scale
-  per cached token (the k_rope_scales overload).
+  per cached token (the k_rope_scales overload); K_nope with one scale per
+  tensor or, where the split-Q overload's k_scales hold one per token, one
+  per K row.
 
 Readings where the pages are silent:
 * cache_lens[b] is the prior length; the query tokens of sequence b sit at
@@ -45,9 +47,20 @@ def _raw(t: torch.Tensor, fp8: bool) -> np.ndarray:
 
 
 def _decode(raw: np.ndarray, fp8: bool, scale) -> np.ndarray:
+    """Real values of raw codes: bf16 bits, or e4m3 codes times their scale
+    (a number, or one scale per leading row of `raw`)."""
     if fp8:
-        return decode_e4m3(raw) * float(scale)
+        s = np.asarray(scale, dtype=np.float64)
+        return decode_e4m3(raw) * (s.reshape((-1,) + (1,) * (raw.ndim - 1)) if s.ndim else float(s))
     return decode_bf16(raw)
+
+
+def k_scale_rows(w, rows):
+    """K_nope dequantisation scale of K rows `rows`: the per-tensor scale, or
+    (one scale per K row, the split-Q overload's k_scales) the rows' own."""
+    if w.k_scale is None or np.ndim(w.k_scale) == 0:
+        return w.k_scale
+    return np.asarray(w.k_scale, dtype=np.float64).reshape(-1)[rows]
 
 
 def gather_k_rope(w, b: int) -> np.ndarray:
@@ -115,7 +128,7 @@ def reference(w, heads=None, rows=None, row_block=1024, out=None, q=None):
         j = np.arange(L)
         for h in heads:
             k_full = np.empty((L, NOPE + ROPE), dtype=np.float64)
-            k_full[:, :NOPE] = _decode(k_raw[G:G + L, h, :], fp8, w.k_scale)
+            k_full[:, :NOPE] = _decode(k_raw[G:G + L, h, :], fp8, k_scale_rows(w, np.arange(G, G + L)))
             k_full[:, NOPE:] = k_rope
             v = _decode(v_raw[G:G + L, h, :], fp8, w.v_scale)
             for s0 in range(0, sel.size, row_block):

@@ -25,7 +25,7 @@ that compares the two also checks the buffer packing.
 """
 import numpy as np
 
-from .attention import DV, NOPE, ROPE, _decode, _raw, gather_k_rope
+from .attention import DV, NOPE, ROPE, _decode, _raw, gather_k_rope, k_scale_rows
 
 
 def window_reference(w, buffer_row_offsets, cache_offsets, heads=None):
@@ -61,7 +61,7 @@ def window_reference(w, buffer_row_offsets, cache_offsets, heads=None):
             allowed = np.ones((n, W), dtype=bool)
         for h in heads:
             k = np.empty((W, NOPE + ROPE), dtype=np.float64)
-            k[:, :NOPE] = _decode(k_raw[G + a, h, :], fp8, w.k_scale)
+            k[:, :NOPE] = _decode(k_raw[G + a, h, :], fp8, k_scale_rows(w, G + a))
             k[:, NOPE:] = rope
             v = _decode(v_raw[G + a, h, :], fp8, w.v_scale)
             qh = _decode(q_raw[q0:q0 + n, h, :], fp8, w.q_scale)

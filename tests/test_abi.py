@@ -112,6 +112,42 @@ def test_fp8_needs_scales(lib):
     assert _call_ragged(lib, mixed) == binding.MLA_ERR_INVALID_ARG
 
 
+def test_fp8_per_token_k_scales(lib):
+    """K_nope may carry one scale per K row; the workspace then holds the
+    converted K_rope at the K rows (S_k rows, not the pool's slots), and the
+    split overload's v needs a scale of its own."""
+    fp8 = binding.MLA_DTYPE_FP8_E4M3
+    a = _ragged_args(q=_desc([10, 2, 192], fp8), k=_desc([20, 2, 128], fp8),
+                     v=_desc([20, 2, 128], fp8), rope=_desc([4, 16, 64], fp8))
+    for t, gran in ((a["q"], binding.MLA_SCALE_PER_TENSOR), (a["k"], binding.MLA_SCALE_PER_TOKEN),
+                    (a["v"], binding.MLA_SCALE_PER_TENSOR), (a["rope"], binding.MLA_SCALE_PER_TOKEN)):
+        t.scale = 0x50000
+        t.scale_gran = gran
+    a["ws_bytes"] = binding.workspace_size(2, fp8_pool_slots=19)      # one row short of S_k = 20
+    assert _call_ragged(lib, a) == binding.MLA_ERR_INVALID_ARG
+    assert b"workspace too small" in lib.mla_last_error_string()
+    a["ws_bytes"] = binding.workspace_size(2, fp8_pool_slots=20)      # less than the 64 pool slots
+    assert _call_ragged(lib, a) != binding.MLA_ERR_INVALID_ARG        # host checks pass
+    a["k"].scale_gran = binding.MLA_SCALE_PER_TENSOR                   # per tensor: 64 rows needed
+    assert _call_ragged(lib, a) == binding.MLA_ERR_INVALID_ARG
+    a["k"].scale_gran = binding.MLA_SCALE_NONE
+    assert _call_ragged(lib, a) == binding.MLA_ERR_INVALID_ARG
+    assert b"k_nope" in lib.mla_last_error_string()
+
+    # Split Q: per-token k and a v without its own scale.
+    a["k"].scale_gran = binding.MLA_SCALE_PER_TOKEN
+    a["v"].scale = None
+    a["v"].scale_gran = binding.MLA_SCALE_NONE
+    r = lambda d: None if d is None else ctypes.byref(d)
+    qn, qr = _desc([10, 2, 128], fp8), _desc([10, 2, 64])
+    qn.scale, qn.scale_gran = 0x50000, binding.MLA_SCALE_PER_TENSOR
+    st = lib.mla_prefill_ragged_split(r(a["out"]), r(qn), r(qr), r(a["k"]), r(a["v"]), r(a["rope"]),
+                                      r(a["pt"]), 2, a["ro"], a["cl"], a["scale"], a["mask"], a["ws"],
+                                      a["ws_bytes"], None)
+    assert st == binding.MLA_ERR_INVALID_ARG
+    assert b"fp8 v" in lib.mla_last_error_string()
+
+
 def test_ragged_rejects_unaligned_stride(lib):
     q = _desc([10, 2, 192])
     q.stride[1] = 196          # 392 bytes: not a multiple of 16

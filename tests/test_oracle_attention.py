@@ -34,7 +34,8 @@ def _sdpa_reference(w):
     if fp8:
         deq = lambda t, s: _f64(t.view(torch.float8_e4m3fn)) * s
         q = deq(w.q, w.q_scale)
-        kn = deq(w.k_nope, w.k_scale)
+        ks = np.asarray(w.k_scale, dtype=np.float64)   # per tensor, or one per K row
+        kn = deq(w.k_nope, torch.from_numpy(ks)[:, None, None] if ks.ndim else float(ks))
         v = deq(w.v, w.v_scale)
         pool = _f64(w.k_rope_pool.view(torch.float8_e4m3fn)) * _f64(w.k_rope_scales)[..., None]
     else:
@@ -73,6 +74,41 @@ def test_matches_standard_mha_with_replicated_rope(dtype, mask):
     sdpa = _sdpa_reference(w)
     assert np.isfinite(ref).all()
     np.testing.assert_allclose(ref, sdpa, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("mask", ["causal", "null"])
+def test_per_token_k_scales_match_standard_mha(mask):
+    """One K_nope scale per K row (rows re-quantised over a 2^±2 spread): the
+    oracle's per-row dequantisation against SDPA on torch-dequantised keys."""
+    w = workloads.per_token_k(workloads.custom([5, 1, 0, 9], [0, 3, 2, 6], heads=3, page_size=4,
+                                               dtype="fp8", seed=8, mask=mask))
+    assert np.ndim(w.k_scale) == 1 and len(np.unique(w.k_scale)) > w.total_k // 2
+    np.testing.assert_allclose(oatt.reference(w), _sdpa_reference(w), rtol=1e-12, atol=1e-12)
+
+
+def test_per_token_k_scales_equal_reduce_to_per_tensor():
+    from dataclasses import replace
+    w = workloads.custom([7, 3], [2, 5], heads=2, page_size=4, dtype="fp8", seed=9)
+    wt = replace(w, k_scale=np.full(w.total_k, w.k_scale, dtype=np.float32))
+    assert np.array_equal(oatt.reference(w), oatt.reference(wt))
+
+
+def test_per_token_k_scale_of_one_row_reaches_only_its_viewers():
+    """Changing key row t's scale changes exactly the query rows that see it
+    (causal: its own sequence's rows at or after its position)."""
+    from dataclasses import replace
+    w = workloads.per_token_k(workloads.custom([6, 5], [3, 2], heads=2, page_size=4, dtype="fp8",
+                                               seed=10))
+    G1 = int(w.n[0] + w.prior[0])
+    t = G1 + 4                                  # sequence 1, context position 4
+    ks = np.array(w.k_scale, copy=True)
+    ks[t] *= 3.0
+    a, b = oatt.reference(w), oatt.reference(replace(w, k_scale=ks))
+    changed = np.abs(a - b).max(axis=(1, 2)) > 0
+    q1 = int(w.row_offsets[1])
+    expect = np.zeros(w.total_q, dtype=bool)
+    expect[q1 + (4 - int(w.prior[1])):] = True  # query i sees position 4 when prior + i >= 4
+    assert np.array_equal(changed, expect)
 
 
 def test_tiny_config_matches_standard_mha():

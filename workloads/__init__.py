@@ -97,7 +97,7 @@ class Workload:
     page_table: np.ndarray     # uint32 [B, max_pages]
     scale: float               # softmax scale applied to QK^T
     q_scale: Optional[float] = None
-    k_scale: Optional[float] = None
+    k_scale: Optional[object] = None   # float, or float32 [S_k] (one scale per K row)
     v_scale: Optional[float] = None
     k_rope_scales: Optional[torch.Tensor] = None  # float32 [num_pages, P]
     extra: dict = field(default_factory=dict)
@@ -306,10 +306,28 @@ def device_inputs(w: Workload, device="cuda", pin=False):
     }
     if w.spec.dtype == "fp8":
         d["q_scale"] = mv(torch.tensor([w.q_scale], dtype=torch.float32))
-        d["k_scale"] = mv(torch.tensor([w.k_scale], dtype=torch.float32))
+        d["k_scale"] = mv(torch.from_numpy(np.atleast_1d(np.asarray(w.k_scale, dtype=np.float32)).copy()))
         d["v_scale"] = mv(torch.tensor([w.v_scale], dtype=torch.float32))
         d["k_rope_scales"] = mv(w.k_rope_scales)
     return d
+
+
+def per_token_k(w: Workload, spread_log2: float = 2.0) -> Workload:
+    """The fp8 workload `w` with K_nope re-quantised per K row: row t's real
+    values (code * k_scale) are multiplied by 2^u_t, u_t ~ U(-spread_log2,
+    spread_log2) from a generator of its own (seed + 20011), then cast to e4m3
+    with the row's own scale amax_row / 448 (saturating, round to nearest
+    even).  Every other tensor is w's.  k_scale becomes float32 [S_k]."""
+    assert w.spec.dtype == "fp8", "per-token K scales are for fp8 workloads"
+    rng = np.random.Generator(np.random.PCG64(w.spec.seed + 20011))
+    Sk = w.total_k
+    factor = np.exp2(rng.uniform(-spread_log2, spread_log2, size=Sk)).astype(np.float32)
+    real = w.k_nope.view(torch.float8_e4m3fn).float().numpy() * np.float32(w.k_scale)
+    real = real.reshape(Sk, -1) * factor[:, None]
+    amax = np.abs(real).max(axis=1) if Sk else np.zeros(0, np.float32)
+    row_scale = np.where(amax > 0, amax / np.float32(FP8_MAX), np.float32(1.0)).astype(np.float32)
+    codes = _sat_e4m3((real / row_scale[:, None]).astype(np.float32)).view(w.k_nope.shape)
+    return replace(w, k_nope=codes, k_scale=row_scale)
 
 
 def contiguous_rope(w: Workload):
