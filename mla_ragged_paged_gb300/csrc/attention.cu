@@ -1047,7 +1047,7 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
         // warp of the group has finished reading tile j-1's; the load for
         // tile j+1 is issued here and consumed a tile later.
         if (kt > 0 && !mbar_wait(ks_free, (kt - 1) & 1u, abort)) return;
-        asm volatile("st.shared.f32 [%0], %1;" ::"r"(ks_row + 4u * r), "f"(ks_next) : "memory");
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(ks_row + 4u * r), "f"(ks_next * sl2) : "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(ks_full);
         if (!mbar_wait(ks_full, kt & 1u, abort)) return;
@@ -1064,9 +1064,14 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s.s_free[q]));
+      // Exponent reference so far (0 before the first visible key).
+      float mb = m_used == -INFINITY ? 0.f : m_used;
       if (KTOK) {
-        // Column c of S times its key's scale (a broadcast read: every lane
-        // reads the same four scales).
+        // Per-token K scales: column c's factor sl2 * s_k[key] (a broadcast
+        // read: every lane reads the same four) goes into the one FMA that
+        // also subtracts the current reference, y = S * factor + 6 - mb; the
+        // max below is then taken over y.
+        const uint64_t off = f2_pack(C::kPScaleLog2 - mb, C::kPScaleLog2 - mb);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -1076,10 +1081,10 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
                          : "=f"(k0), "=f"(k1), "=f"(k2), "=f"(k3)
                          : "r"(ks_row + 4u * (32 * c + 4 * k)));
             float x0, x1, x2, x3;
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[c][4 * k]), __uint_as_float(sr[c][4 * k + 1])),
-                             f2_pack(k0, k1)), x0, x1);
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[c][4 * k + 2]), __uint_as_float(sr[c][4 * k + 3])),
-                             f2_pack(k2, k3)), x2, x3);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][4 * k]), __uint_as_float(sr[c][4 * k + 1])),
+                             f2_pack(k0, k1), off), x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][4 * k + 2]), __uint_as_float(sr[c][4 * k + 3])),
+                             f2_pack(k2, k3), off), x2, x3);
             sr[c][4 * k] = __float_as_uint(x0);
             sr[c][4 * k + 1] = __float_as_uint(x1);
             sr[c][4 * k + 2] = __float_as_uint(x2);
@@ -1106,7 +1111,9 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
 #pragma unroll
         for (int e = 0; e < 32; e += 2)
           smax = max3(smax, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-      const float m_tile = smax == -INFINITY ? -INFINITY : smax * sl2;
+      const float m_tile = smax == -INFINITY ? -INFINITY
+                           : KTOK           ? smax - C::kPScaleLog2 + mb
+                                            : smax * sl2;
       const float m_new = fmaxf(m_used, m_tile);
       const bool grow = m_new > m_used + C::kThreshold;
       float alpha = 1.f;
@@ -1114,8 +1121,22 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
         alpha = ex2_approx(m_used - m_new);
         m_used = m_new;
         l *= alpha;
+        if (KTOK) {
+          // Move this tile's exponents to the new reference.
+          const float d = mb - m_used;
+          const uint64_t d2 = f2_pack(d, d);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float x0, x1;
+              f2_unpack(f2_add(f2_pack(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), d2), x0, x1);
+              sr[c][e] = __float_as_uint(x0);
+              sr[c][e + 1] = __float_as_uint(x1);
+            }
+        }
       }
-      const float mb = m_used == -INFINITY ? 0.f : m_used;
+      mb = m_used == -INFINITY ? 0.f : m_used;
       const uint64_t negm = f2_pack(C::kPScaleLog2 - mb, C::kPScaleLog2 - mb);
       uint64_t lacc = f2_pack(0.f, 0.f);
 #pragma unroll
@@ -1125,8 +1146,13 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
         for (int e = 0; e < 16; ++e) {
           const int col = 32 * c + 2 * e;
           float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])),
-                           sl2x2, negm), x0, x1);
+          if (KTOK) {
+            x0 = __uint_as_float(sr[c][2 * e]);
+            x1 = __uint_as_float(sr[c][2 * e + 1]);
+          } else {
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])),
+                             sl2x2, negm), x0, x1);
+          }
           float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           if (masked) {
             p0 = col < nvalid ? p0 : 0.f;
