@@ -231,7 +231,11 @@ def run_reference(args, world, rank):
     """The CPU oracle on host cores; under torchrun only rank 0 runs it."""
     if rank != 0:
         return
-    w = workloads.generate(workloads.config(args.workload))
+    spec = workloads.config(args.workload)
+    w = workloads.generate(spec)
+    ktok = spec.dtype == "fp8" and args.k_scales == "token"
+    if ktok:
+        w = workloads.per_token_k(w)
     per_step = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
     rows, nh = oracle_shape_for(w, per_step)
     for i in range(args.warmup):
@@ -246,11 +250,15 @@ def run_reference(args, world, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "sample_per_step": "query rows of one (sequence, head)"},
+            "config": {"workload": f"{spec.name}: {spec.description}",
+                       "sample_per_step": "query rows of one (sequence, head)"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(),
                              "kind": "oracle", "sample": f"per step: {sample}"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+    if spec.dtype == "fp8":
+        line["config"]["k_scales"] = ("one K_nope scale per K row (re-quantised per row)" if ktok
+                                      else "per-tensor K_nope scale")
     print(json.dumps(line), flush=True)
 
 
