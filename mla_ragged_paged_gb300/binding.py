@@ -108,12 +108,24 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _on_device(t, what="tensor"):
+    """Every array the library reads or writes is device memory: a host
+    tensor's address handed to a kernel would be an illegal access, so refuse
+    it here."""
+    if not t.is_cuda:
+        raise MlaError(MLA_ERR_INVALID_ARG, f"{what} must be a CUDA tensor (got {t.device})")
+    return t
+
+
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else ctypes.c_void_p(_on_device(t).data_ptr())
 
 
 def describe(t, dtype, scale=None, scale_gran=MLA_SCALE_NONE):
-    """MlaTensor for a torch tensor (element strides, up to 4 dims)."""
+    """MlaTensor for a CUDA torch tensor (element strides, up to 4 dims)."""
+    _on_device(t)
+    if scale is not None:
+        _on_device(scale, "scale")
     d = MlaTensor()
     d.data = t.data_ptr()
     d.dtype = dtype

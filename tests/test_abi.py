@@ -304,3 +304,15 @@ def test_split_rejects_bad_arguments(lib, case):
                                       a["ws_bytes"], None)
     assert st == binding.MLA_ERR_INVALID_ARG
     assert lib.mla_last_error_string()
+
+
+def test_binding_refuses_host_tensors():
+    """A host tensor's address must never reach a kernel: the binding raises
+    before any call."""
+    import torch
+    t = torch.zeros(4, 2, 192, dtype=torch.bfloat16)
+    with pytest.raises(binding.MlaError, match="CUDA tensor"):
+        binding.describe(t, binding.MLA_DTYPE_BF16)
+    with pytest.raises(binding.MlaError, match="CUDA tensor"):
+        binding._ptr(torch.zeros(3, dtype=torch.int32))
+    assert binding._ptr(None) is None
