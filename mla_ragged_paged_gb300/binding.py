@@ -406,7 +406,9 @@ def merge(out, partial_out, partial_lse, row_offsets, buffer_row_offsets, stream
     """mla_prefill_merge over rows 0..R-1 (R = partial_out.shape[0]);
     buffer_row_offsets is the plan's [R_max, B+1] array."""
     B = row_offsets.numel() - 1
-    assert buffer_row_offsets.shape[-1] == B + 1 and buffer_row_offsets.stride(0) == B + 1
+    if buffer_row_offsets.shape[-1] != B + 1 or (buffer_row_offsets.dim() > 1
+                                                  and buffer_row_offsets.stride(0) != B + 1):
+        raise MlaError(MLA_ERR_INVALID_ARG, "buffer_row_offsets must hold rows of B+1 packed offsets")
     d_out = describe(out, MLA_DTYPE_BF16)
     d_po = describe(partial_out, MLA_DTYPE_BF16)
     d_pl = describe(partial_lse, MLA_DTYPE_F32)
