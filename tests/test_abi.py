@@ -316,3 +316,9 @@ def test_binding_refuses_host_tensors():
     with pytest.raises(binding.MlaError, match="CUDA tensor"):
         binding._ptr(torch.zeros(3, dtype=torch.int32))
     assert binding._ptr(None) is None
+
+
+def test_ragged_rejects_batch_above_limit(lib):
+    a = _ragged_args(pt=_desc([4097, 2], binding.MLA_DTYPE_U32))
+    assert _call_ragged(lib, a) == binding.MLA_ERR_INVALID_ARG
+    assert b"4096" in lib.mla_last_error_string()

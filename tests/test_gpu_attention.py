@@ -177,3 +177,17 @@ def test_many_launches_stable(lib, name, calls):
         assert binding.device_status(ws) == 0, f"launch {i}"
         if i % 20 == 19:
             assert torch.equal(outs[0], outs[1]), f"launch {i}"
+
+
+@pytest.mark.parametrize("B,dtype", [(2048, "bf16"), (2049, "fp8"), (4096, "bf16")])
+def test_largest_batches(lib, B, dtype):
+    """Batch sizes around the scheduler's longest-first sort (up to 2048
+    sequences; identity order above) and at the 4096-sequence limit, with
+    empty sequences mixed in, every sequence checked."""
+    rng = np.random.default_rng(B)
+    n = rng.integers(0, 9, size=B)
+    prior = rng.integers(0, 21, size=B) * (rng.random(B) < 0.7)
+    w = workloads.custom(n.tolist(), prior.tolist(), heads=1, page_size=16, seed=B, dtype=dtype)
+    got, status = run_gpu(w)
+    assert status == 0
+    assert_close(got, oatt.reference(w), f"B={B}", *tol(w))
