@@ -171,6 +171,17 @@ def dist_max(x, world):
     return float(t.item())
 
 
+def dist_sum(x, world):
+    """Sum of x over the ranks (work units every rank processed)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -434,6 +445,9 @@ def main():
         t_end.record(stream)
         barrier(world)
     total_ms = dist_max(t_start.elapsed_time(t_end), world)
+    # Every rank's batch is drawn with its own seed: the whole job's work is
+    # the sum of the ranks' causal-effective flops.
+    F_all = dist_sum(float(F), world)
     # Attention-kernel span (the per-row calls in chunked mode) and merge span.
     seg = {k: v / args.steps for k, v in tk.totals().items()}   # ms per step per segment
     attn_ms = seg["attn"]
@@ -540,7 +554,7 @@ def main():
                        "ms": seg["gather"], "kernel": "gather_kernel", "bytes_per_step": gb}}
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and not latent:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not latent:
         # About 10-30 s of host work: size from a short probe, then widen the
         # head sample once if the first run came in under 10 s.
         rows, nh = oracle_shape_for(w, 15.0)
@@ -562,14 +576,14 @@ def main():
         launches_per_step += 1                 # merge
     merge_txt = "" if fold else " + mla_prefill_merge"
     if rank == 0:
-        value = world * F * args.steps / (total_ms * 1e-3) / 1e12
+        value = F_all * args.steps / (total_ms * 1e-3) / 1e12
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if fp8 else "bf16",
             "data": "synthetic",
             "config": {"workload": f"{spec.name}: {spec.description}", "global_batch": B * world,
-                       "total_q_tokens": Tq, "heads": H, "causal_effective_tflop_per_step": F / 1e12,
+                       "total_q_tokens": Tq, "heads": H, "causal_effective_tflop_per_step": F_all / 1e12,
                        "parallelism": f"dp{world} (independent batches)" if world > 1 else "none",
                        "l2": f"inputs ({in_bytes / 1e9:.2f} GB) larger than L2; no flush",
                        "step": ("mla_prefill_plan + %d x (mla_gather_rows + 2 x mla_up_project + "
@@ -582,7 +596,7 @@ def main():
                                 if split else "mla_prefill_plan + mla_prefill_ragged")},
             "pct_of_peak": 100.0 * value / world / peak,
             "clocks": clocks,
-            "e2e": {"value": world * F * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "e2e": {"value": F_all * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "pipelining": "two buffer sets: H2D of step i+1 and D2H of step i-1 overlap step i"},
             "gpu_launches": launches_per_step * args.steps,

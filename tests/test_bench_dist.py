@@ -1,5 +1,5 @@
 """bench.py's multi-rank host logic on CPU with gloo, world size 2: the
-max-over-ranks step time, the per-rank workload seeds, and a torchrun launch
+max-over-ranks step time, the sum of the ranks' work, the per-rank workload seeds, and a torchrun launch
 of the reference arm (rank 0 alone prints one JSON line, the other rank exits
 0 without work)."""
 import json
@@ -30,9 +30,10 @@ def _rank_main(rank, world, port, out):
     w, r, _ = bench.dist_setup()
     assert (w, r) == (world, rank)
     m = bench.dist_max(1.5 + rank, world)
+    total = bench.dist_sum(10.0 + rank, world)
     bench.barrier(world)
     spec = bench.rank_spec(workloads.config("tiny_bf16"), rank)
-    out.put((rank, m, spec.seed))
+    out.put((rank, m, spec.seed, total))
     import torch.distributed as dist
     dist.destroy_process_group()
 
@@ -48,8 +49,9 @@ def test_dist_helpers_gloo_world_2():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    assert [m for _, m, _ in res] == [2.5, 2.5]          # the max over ranks, seen by both
+    assert [m for _, m, _, _ in res] == [2.5, 2.5]       # the max over ranks, seen by both
     assert res[0][2] != res[1][2]                          # each rank draws its own batch
+    assert [t for _, _, _, t in res] == [21.0, 21.0]       # work summed over ranks
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="host-side launch test (no GPU use)")
