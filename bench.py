@@ -309,7 +309,12 @@ def main():
 
     import mla_ragged_paged_gb300 as pkg
     from mla_ragged_paged_gb300 import binding
-    pkg.build()
+    # One rank compiles (if the library is stale); the others wait for it.
+    if local == 0:
+        pkg.build()
+    barrier(world)
+    if local != 0:
+        pkg.build()          # up to date by now: returns at once
     binding.load()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
