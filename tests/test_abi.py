@@ -322,3 +322,17 @@ def test_ragged_rejects_batch_above_limit(lib):
     a = _ragged_args(pt=_desc([4097, 2], binding.MLA_DTYPE_U32))
     assert _call_ragged(lib, a) == binding.MLA_ERR_INVALID_ARG
     assert b"4096" in lib.mla_last_error_string()
+
+
+def test_binding_k_scale_granularity_and_workspace_rows():
+    """Host logic of the binding: a one-float k_scale is per tensor, a longer
+    one per K row; fp8 workspaces then hold one converted K_rope row per K row
+    instead of one per pool slot."""
+    import torch
+    k_nope = torch.empty(20, 2, 128, dtype=torch.uint8)
+    assert not binding._per_token(None)
+    assert not binding._per_token(torch.ones(1))
+    assert binding._per_token(torch.ones(20))
+    assert binding._rope_rows(k_nope, torch.ones(1), 64) == 64
+    assert binding._rope_rows(k_nope, torch.ones(20), 64) == 20
+    assert binding.workspace_size(3, fp8_pool_slots=20) == binding.workspace_size(3) + 20 * 128
