@@ -13,7 +13,11 @@
  *
  * Conventions shared by every entry point:
  *   - Every pointer marked "device" is caller-owned device memory; the library
- *     never allocates or frees device memory and keeps no per-call state.
+ *     never allocates or frees device memory and keeps no per-call state.  The
+ *     one exception is mla_prefill_ragged_noalloc: its scheduler workspace is
+ *     a fixed 33,024-byte device array inside the library, held on every GPU
+ *     that loads it until process exit and shared by all calls of that entry
+ *     point.
  *   - Calls are asynchronous on `stream`; none synchronises except
  *     mla_read_device_status, which says so.  Descriptor structs are host
  *     memory read during the call only.
@@ -101,9 +105,10 @@ typedef struct {
  *   cache_offsets      device uint32 [max_buffer_rows, batch]   (written)
  *   buffer_lengths     device int32  [max_buffer_rows]          (written)
  *   num_rows           device uint32 [1] or NULL: receives R; rows past
- *                      max_buffer_rows are not written.  If S does not fit in
- *                      32 bits it receives 0xFFFFFFFF and the outputs are
- *                      unspecified.
+ *                      max_buffer_rows are not written.  It receives
+ *                      0xFFFFFFFF, and the outputs are unspecified, when S does
+ *                      not fit in 32 bits or input_row_offsets decreases
+ *                      somewhere (a negative new-token count).
  * One kernel launch, no host synchronisation.
  */
 mla_status_t mla_prefill_plan(const uint32_t* input_row_offsets, const uint32_t* cache_lens,
@@ -248,11 +253,16 @@ mla_status_t mla_prefill_ragged_split(const mla_tensor_t* out, const mla_tensor_
  *   - The scheduler workspace is a fixed device array inside the library
  *     (33,024 bytes, room for 1024 sequences) that every GPU loading the
  *     library keeps until process exit.  A batch above 1024 returns
- *     MLA_ERR_INVALID_ARG, and so do fp8 inputs, whose K_rope conversion
- *     needs more room than the array has.
+ *     MLA_ERR_INVALID_ARG, and so do fp8 inputs (any of q, k_nope, v,
+ *     k_rope_pages), whose K_rope conversion needs more room than the array
+ *     has.
  *   - The first call on a device looks the array's address up with
  *     cudaGetSymbolAddress (one-time set-up with that device current); make
  *     that first call before any stream capture.  Later calls only launch.
+ *     The address is kept together with the id of the device's current
+ *     context; after cudaDeviceReset (a new primary context, the array at a
+ *     new address) the next call repeats the set-up, so make that call
+ *     before any stream capture too.
  *   - No cudaMalloc, cudaFree or other allocating call is made.
  *   - All calls share the one array and each call rewrites what it needs, so
  *     calls whose kernels can overlap on the GPU (different streams without

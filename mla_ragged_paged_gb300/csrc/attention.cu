@@ -45,6 +45,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "host_common.h"
 #include "sm103.cuh"
@@ -1772,7 +1773,45 @@ namespace {
 constexpr uint32_t kNoAllocMaxBatch = 1024;
 constexpr size_t kNoAllocBytes = sizeof(WsHeader) + kNoAllocMaxBatch * sizeof(SeqRec);
 static_assert(kNoAllocBytes % 256 == 0, "workspace size must keep 256-byte granularity");
-std::atomic<void*> g_noalloc_addr[64];
+
+// The array's device address belongs to the context that loaded the module:
+// a cudaDeviceReset (or any other re-creation of the device's primary
+// context) moves it.  So the address is cached per device together with the
+// id of the context it was looked up in, and looked up again when the
+// current context's id differs.
+struct NoAllocSlot {
+  std::mutex m;
+  unsigned long long ctx_id = 0;
+  void* addr = nullptr;
+};
+NoAllocSlot g_noalloc[64];
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+PfnCtxGetCurrent g_ctx_get_current = nullptr;
+PfnCtxGetId g_ctx_get_id = nullptr;
+std::once_flag g_ctx_fn_once;
+
+// Id of the calling thread's current context, 0 if none is current (the
+// runtime creates the primary context lazily) or the driver lacks the query.
+unsigned long long current_ctx_id() {
+  std::call_once(g_ctx_fn_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<PfnCtxGetCurrent>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = reinterpret_cast<PfnCtxGetId>(fn);
+  });
+  if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 }  // namespace
 }  // namespace mla
 
@@ -1792,18 +1831,36 @@ extern "C" mla_status_t mla_prefill_ragged_noalloc(const mla_tensor_t* out, cons
                 "batch %lld exceeds the %u sequences the built-in workspace of "
                 "mla_prefill_ragged_noalloc holds; use mla_prefill_ragged with a workspace",
                 (long long)page_table->shape[0], kNoAllocMaxBatch);
+  // fp8 inputs convert the whole K_rope pool into the workspace first, which
+  // the fixed array has no room for.
+  const mla_tensor_t* ins[4] = {q, k_nope, v, k_rope_pages};
+  for (const mla_tensor_t* t : ins)
+    if (t && t->dtype == MLA_DTYPE_FP8_E4M3)
+      return fail(MLA_ERR_INVALID_ARG,
+                  "mla_prefill_ragged_noalloc takes bf16 inputs only; fp8 inputs need "
+                  "mla_prefill_ragged with a workspace");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= 64) return fail(MLA_ERR_UNSUPPORTED, "device index %d", dev);
-  // One-time set-up per device (the device is current here): the array's
-  // host-side name is only a stand-in, so ask the runtime for its address.
-  void* ws = g_noalloc_addr[dev].load(std::memory_order_acquire);
-  if (!ws) {
-    e = cudaGetSymbolAddress(&ws, g_noalloc_workspace);
-    if (e != cudaSuccess || !ws)
-      return fail(MLA_ERR_CUDA, "cudaGetSymbolAddress(workspace): %s", cudaGetErrorString(e));
-    g_noalloc_addr[dev].store(ws, std::memory_order_release);
+  // Set-up, once per device and context (the device is current here): the
+  // array's host-side name is only a stand-in, so ask the runtime for its
+  // address.
+  void* ws = nullptr;
+  {
+    NoAllocSlot& slot = g_noalloc[dev];
+    std::lock_guard<std::mutex> lock(slot.m);
+    const unsigned long long id = current_ctx_id();
+    if (id != 0 && id == slot.ctx_id && slot.addr) {
+      ws = slot.addr;
+    } else {
+      e = cudaGetSymbolAddress(&ws, g_noalloc_workspace);
+      if (e != cudaSuccess || !ws)
+        return fail(MLA_ERR_CUDA, "cudaGetSymbolAddress(workspace): %s", cudaGetErrorString(e));
+      // The lookup made the primary context current if it was not yet.
+      slot.ctx_id = current_ctx_id();
+      slot.addr = ws;
+    }
   }
   // The scheduler launch inside rewrites every workspace field the attention
   // kernel reads (header, work counter, sequence records) on each call.
