@@ -291,7 +291,7 @@ def main():
     ap.add_argument("--mode", default="full", choices=["full", "chunked", "contiguous", "latent", "split"],
                     help="full-context attention call (paged K_rope); one call per plan buffer row "
                          "plus the merge; the full-context call on a contiguous K_rope; or the "
-                         "latent-cache path (per row: gather, K/V up-projection, attention; merge); "
+                         "latent-cache path (per row: gather fused with the K/V up-projection, attention; fold or merge); "
                          "or Q split into q_nope and a bf16 q_rope")
     ap.add_argument("--k-scales", default="tensor", choices=["tensor", "token"],
                     help="fp8 workloads: one K_nope scale per tensor, or one per K row (the "
@@ -373,7 +373,7 @@ def main():
     fold = chunked and args.combine == "fold"
     scratch = binding.chunked_scratch(R, Tq, H, dev) if chunked and not fold else None
     lse_buf = torch.empty((Tq, H), dtype=torch.float32, device=dev) if fold else None
-    lbuf = binding.LatentRowBuffers(T, 576, H, dev) if latent else None
+    lbuf = binding.LatentRowBuffers(T, H, dev) if latent else None
 
     def attention(inp, o, tk=None):
         """The attention part of a step; `tk` (a Ticker) labels its segments."""
@@ -400,21 +400,20 @@ def main():
             lo, hi = r * T, min((r + 1) * T, w.total_k)
             o_r, l_r = (o, lse_buf) if fold else (scratch[0][r], scratch[1][r])
             if latent:
-                # Gather the row's latent rows, project K_nope and V, attend.
+                # The row's K_nope and V projected from its gathered latent
+                # rows (one launch), then its attention with K_rope read from
+                # the latent cache through the page table.
                 n = hi - lo
-                rows = lbuf.rows[:n]
-                tick("gather")
-                binding.gather_rows(rows, inp["latent_pool"], inp["page_table"], plan_out[0][r],
-                                    plan_out[1][r], stream=stream)
                 tick("gemm")
                 kn, vv = lbuf.k_nope[:n], lbuf.v[:n]
-                binding.up_project(kn.view(n, H * 128), rows[:, :512], inp["w_uk"], lbuf.gemm_ws, stream)
-                binding.up_project(vv.view(n, H * 128), rows[:, :512], inp["w_uv"], lbuf.gemm_ws, stream)
+                binding.gather_up_project(kn, vv, inp["latent_pool"], inp["w_uk"], inp["w_uv"],
+                                          inp["page_table"], plan_out[0][r], plan_out[1][r], stream=stream)
                 tick("attn")
-                binding.prefill_ragged_chunk_contiguous(
-                    o_r, l_r, inp["q"], kn, vv, rows[:, 512:576], inp["row_offsets"], inp["cache_lens"],
-                    plan_out[0][r], plan_out[1][r], w.scale, binding.MLA_MASK_CAUSAL, ws, stream=stream,
-                    flags=flags)
+                binding.prefill_ragged_chunk(o_r, l_r, inp["q"], kn, vv,
+                                             binding.latent_rope_pages(inp["latent_pool"]), inp["page_table"],
+                                             inp["row_offsets"], inp["cache_lens"], plan_out[0][r],
+                                             plan_out[1][r], w.scale, binding.MLA_MASK_CAUSAL, ws,
+                                             stream=stream, flags=flags)
                 continue
             row_scales = dict(scales, k_scale=scales["k_scale"][lo:hi]) if ktok else scales
             binding.prefill_ragged_chunk(o_r, l_r, inp["q"], inp["k_nope"][lo:hi], inp["v"][lo:hi],
@@ -544,19 +543,15 @@ def main():
         merge_roofline = {"bound": "hbm", "achieved": m_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                           "frac": m_gbs / peaks["hbm_gbs"], "bytes_per_launch": mbytes,
                           "ms": merge_ms, "kernel": "merge_kernel"}
-    latent_rooflines = None
+    latent_roofline = None
     if latent:
-        # Up-projection: two GEMMs [S, 512] x [512, H*128]; gather: every
-        # context row's 1152 bytes read once and written once.
+        # Gather + up-projection: two GEMMs [S, 512] x [512, H*128] per step,
+        # one launch per buffer row.
         gflop = 2 * 2 * w.total_k * 512 * H * 128
         g_tf = gflop / (seg["gemm"] * 1e-3) / 1e12
-        gb = 2 * w.total_k * 576 * 2
-        latent_rooflines = {
-            "gemm": {"bound": "tensor", "achieved": g_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": g_tf / peaks["bf16_tflops"], "ms": seg["gemm"], "kernel": "cuBLASLt (library)"},
-            "gather": {"bound": "hbm", "achieved": gb / (seg["gather"] * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
-                       "unit": "GB/s", "frac": gb / (seg["gather"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                       "ms": seg["gather"], "kernel": "gather_kernel", "bytes_per_step": gb}}
+        latent_roofline = {"bound": "tensor", "achieved": g_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                           "frac": g_tf / peaks["bf16_tflops"], "ms": seg["gemm"],
+                           "flop_per_step": gflop, "kernel": "up_project_kernel (gather fused, tcgen05)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not latent:
@@ -572,7 +567,7 @@ def main():
 
     # This library's kernels per step (cuBLASLt's GEMM kernels not counted).
     if latent:
-        launches_per_step = 1 + 3 * R          # plan; per row gather, scheduler, attention
+        launches_per_step = 1 + 3 * R          # plan; per row gather + up-projection, scheduler, attention
     elif chunked:
         launches_per_step = 1 + R * (3 if fp8 else 2)
     else:
@@ -591,8 +586,8 @@ def main():
                        "total_q_tokens": Tq, "heads": H, "causal_effective_tflop_per_step": F_all / 1e12,
                        "parallelism": f"dp{world} (independent batches)" if world > 1 else "none",
                        "l2": f"inputs ({in_bytes / 1e9:.2f} GB) larger than L2; no flush",
-                       "step": ("mla_prefill_plan + %d x (mla_gather_rows + 2 x mla_up_project + "
-                                "mla_prefill_ragged_chunk_contiguous) (T=%d)%s" % (R, T, merge_txt))
+                       "step": ("mla_prefill_plan + %d x (mla_gather_up_project + "
+                                "mla_prefill_ragged_chunk, K_rope from the latent cache) (T=%d)%s" % (R, T, merge_txt))
                                if latent else
                                ("mla_prefill_plan + %d x mla_prefill_ragged_chunk (T=%d)%s"
                                 % (R, T, merge_txt)) if chunked else
@@ -620,8 +615,7 @@ def main():
         if merge_roofline is not None:
             line["roofline_merge"] = merge_roofline
         if latent:
-            line["roofline_gemm"] = latent_rooflines["gemm"]
-            line["roofline_gather"] = latent_rooflines["gather"]
+            line["roofline_gemm"] = latent_roofline
             line["segments_ms"] = seg
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -395,21 +395,62 @@ mla_status_t mla_gather_rows(const mla_tensor_t* dst, const mla_tensor_t* cache,
 
 /*
  * Up-projection of latent rows (the step between the gather and the
- * attention when K_nope and V are not cached; the weights are the caller's):
+ * attention when the cache holds the compressed latent row rather than K_nope
+ * and V: mla_prefill_v2_ragged Args: v, "the nope segment of the latent
+ * cache"; the weights are the caller's):
  *   out[t, n] = sum_k latent[t, k] * weight[n, k]
  *   out     device bf16 [rows, N] (e.g. K_nope [rows, H, 128] viewed as
- *           [rows, H * 128])
+ *           [rows, H * 128]), row stride a multiple of 16 bytes
  *   latent  device bf16 [rows, K] (row stride may exceed K: the c_kv
  *           columns of gathered latent rows)
  *   weight  device bf16 [N, K] (nn.Linear layout)
- *   workspace / workspace_bytes  device scratch for the GEMM (0 allowed;
- *           32 MiB lets the library pick its fastest kernels)
- * Rows of every operand must start 16-byte aligned.  A plain dense GEMM run
- * through cuBLASLt (fp32 accumulation, bf16 output).
+ *   status  device uint32 or NULL: MLA_DEVICE_STATUS_TIMEOUT is ORed in if a
+ *           pipeline wait of the kernel gives up
+ * Rows of every operand must start 16-byte aligned.  One launch of this
+ * library's tensor-core GEMM (fp32 accumulation in tensor memory, bf16
+ * output, 128 x 256 output tiles); no library GEMM, no workspace.
  */
 mla_status_t mla_up_project(const mla_tensor_t* out, const mla_tensor_t* latent,
-                            const mla_tensor_t* weight, void* workspace, size_t workspace_bytes,
-                            mla_stream_t stream);
+                            const mla_tensor_t* weight, uint32_t* status, mla_stream_t stream);
+
+/*
+ * Gather and up-projection of one buffer row in one launch
+ * (generic_flare_mla_prefill_ragged_paged_plan summary: the plan exists so the
+ * prefill kernel can gather K/V entries into a contiguous buffer; Args:
+ * buffer_row_offsets, cache_offsets; mla_prefill_v2_ragged Args: v, the nope
+ * segment of the latent cache).  For every sequence b and buffer position
+ * t = buffer_row_offsets[b] + i < buffer_row_offsets[b+1], with context
+ * position a = cache_offsets[b] + i and cache row
+ * c = cache[page_table[b, a / P], a % P, 0:kv_lora_rank]:
+ *   k_out[t, n] = sum_k c[k] * w_uk[n, k]
+ *   v_out[t, n] = sum_k c[k] * w_uv[n, k]
+ * The cache rows are fetched through the page table straight into the GEMM's
+ * operand tiles (TMA row gathers); no contiguous copy of the row is made.
+ *   k_out, v_out  device bf16 [rows, N] (e.g. [rows, H, 128] viewed as
+ *                 [rows, H * 128]); positions t >= buffer_row_offsets[B]
+ *                 (and positions whose page id or page-table column is out of
+ *                 range) receive unspecified values.  v_out and w_uv may both
+ *                 be NULL for a single projection.
+ *   cache         device bf16 [num_pages, P, W], W >= kv_lora_rank, pages
+ *                 contiguous (page stride = P x token stride), token stride a
+ *                 multiple of 16 bytes; e.g. DeepSeek-V3's latent row
+ *                 [c_kv 512 | k_rope 64]
+ *   w_uk, w_uv    device bf16 [N, kv_lora_rank] (nn.Linear layout)
+ *   page_table    device uint32 [B, max_pages]
+ *   buffer_row_offsets, cache_offsets  one row of the plan ([B+1], [B])
+ *   kv_lora_rank  K of the projection, a multiple of 8 (512 for DeepSeek-V3)
+ *   status        device uint32 or NULL: an out-of-range page id or page-table
+ *                 column ORs MLA_DEVICE_STATUS_BAD_PAGE / _BAD_COLUMN, a
+ *                 pipeline wait that gives up MLA_DEVICE_STATUS_TIMEOUT
+ * One launch, no host synchronisation.  The row's K_rope needs no copy
+ * either: mla_prefill_ragged_chunk reads it from the same cache as a paged
+ * K_rope whose token stride is the latent row.
+ */
+mla_status_t mla_gather_up_project(const mla_tensor_t* k_out, const mla_tensor_t* v_out,
+                                   const mla_tensor_t* cache, const mla_tensor_t* w_uk,
+                                   const mla_tensor_t* w_uv, const mla_tensor_t* page_table,
+                                   const uint32_t* buffer_row_offsets, const uint32_t* cache_offsets,
+                                   uint32_t kv_lora_rank, uint32_t* status, mla_stream_t stream);
 
 /* Device status bits written into the workspace's first uint32. */
 #define MLA_DEVICE_STATUS_BAD_PAGE 0x1u    /* page id >= num_pages */

@@ -24,6 +24,7 @@ EXPORTS = ["mla_prefill_plan", "mla_prefill_plan_max_rows", "mla_prefill_ragged_
            "mla_prefill_ragged_workspace_size_fp8", "mla_prefill_ragged", "mla_prefill_ragged_noalloc",
            "mla_prefill_ragged_chunk", "mla_prefill_merge", "mla_prefill_ragged_contiguous",
            "mla_prefill_ragged_chunk_contiguous", "mla_gather_rows", "mla_up_project",
+           "mla_gather_up_project",
            "mla_prefill_ragged_split", "mla_test_inject_stall",
            "mla_read_device_status",
            "mla_last_error_string"]
@@ -87,8 +88,10 @@ def load(path=LIB_PATH):
     lib.mla_test_inject_stall.restype = ctypes.c_int
     lib.mla_gather_rows.argtypes = [pt, pt, pt, vp, vp, vp, vp]
     lib.mla_gather_rows.restype = ctypes.c_int
-    lib.mla_up_project.argtypes = [pt, pt, pt, vp, ctypes.c_size_t, vp]
+    lib.mla_up_project.argtypes = [pt, pt, pt, vp, vp]
     lib.mla_up_project.restype = ctypes.c_int
+    lib.mla_gather_up_project.argtypes = [pt, pt, pt, pt, pt, pt, vp, vp, u32, vp, vp]
+    lib.mla_gather_up_project.restype = ctypes.c_int
     lib.mla_read_device_status.argtypes = [vp, ctypes.POINTER(u32), vp]
     lib.mla_read_device_status.restype = ctypes.c_int
     lib.mla_last_error_string.argtypes = []
@@ -360,46 +363,63 @@ def gather_rows(dst, cache, page_table, buffer_row_offsets, cache_offsets, statu
     return dst
 
 
-GEMM_WORKSPACE_BYTES = 32 << 20
-
-
-def up_project(out, latent, weight, workspace=None, stream=None):
+def up_project(out, latent, weight, status=None, stream=None):
     """mla_up_project: out [rows, N] = latent [rows, K] x weight [N, K]^T (bf16)."""
-    if workspace is None:
-        workspace = torch.empty(GEMM_WORKSPACE_BYTES, dtype=torch.uint8, device=out.device)
     d_out = describe(out, MLA_DTYPE_BF16)
     d_lat = describe(latent, MLA_DTYPE_BF16)
     d_w = describe(weight, MLA_DTYPE_BF16)
     _check(load().mla_up_project(ctypes.byref(d_out), ctypes.byref(d_lat), ctypes.byref(d_w),
-                                 _ptr(workspace), workspace.numel(), _stream(stream)))
+                                 _ptr(status), _stream(stream)))
     return out
 
 
+def gather_up_project(k_out, v_out, cache, w_uk, w_uv, page_table, buffer_row_offsets, cache_offsets,
+                      kv_lora_rank=512, status=None, stream=None):
+    """mla_gather_up_project: K_nope and V of one buffer row, projected from the
+    c_kv columns of its cache rows, gathered through the page table inside the
+    GEMM.  k_out / v_out are [rows, N] (or [rows, H, 128]); v_out and w_uv may
+    both be None."""
+    def flat(t):
+        return t.reshape(t.shape[0], -1) if t is not None and t.dim() == 3 else t
+    k_out, v_out = flat(k_out), flat(v_out)
+    d_k = describe(k_out, MLA_DTYPE_BF16)
+    d_v = describe(v_out, MLA_DTYPE_BF16) if v_out is not None else None
+    d_c = describe(cache, MLA_DTYPE_BF16)
+    d_uk = describe(w_uk, MLA_DTYPE_BF16)
+    d_uv = describe(w_uv, MLA_DTYPE_BF16) if w_uv is not None else None
+    d_pt = describe(page_table, MLA_DTYPE_U32)
+    ref = lambda d: ctypes.byref(d) if d is not None else None
+    _check(load().mla_gather_up_project(ctypes.byref(d_k), ref(d_v), ctypes.byref(d_c), ctypes.byref(d_uk),
+                                        ref(d_uv), ctypes.byref(d_pt), _ptr(buffer_row_offsets),
+                                        _ptr(cache_offsets), int(kv_lora_rank), _ptr(status),
+                                        _stream(stream)))
+
+
 class LatentRowBuffers:
-    """Per-row scratch of the latent path: the gathered rows [T, width] and the
-    projected K_nope / V [T, H, 128]."""
-    def __init__(self, T, width, heads, device="cuda"):
-        self.rows = torch.empty((T, width), dtype=torch.bfloat16, device=device)
+    """Per-row scratch of the latent path: the projected K_nope / V [T, H, 128]."""
+    def __init__(self, T, heads, device="cuda"):
         self.k_nope = torch.empty((T, heads, 128), dtype=torch.bfloat16, device=device)
         self.v = torch.empty((T, heads, 128), dtype=torch.bfloat16, device=device)
-        self.gemm_ws = torch.empty(GEMM_WORKSPACE_BYTES, dtype=torch.uint8, device=device)
+
+
+def latent_rope_pages(cache, kv_lora_rank=512):
+    """The K_rope part of a paged latent cache [num_pages, P, W] as a paged
+    K_rope view [num_pages, P, 64] (token stride W)."""
+    return cache[:, :, kv_lora_rank:kv_lora_rank + 64]
 
 
 def prefill_latent_row(po, pl, q, cache, page_table, row_offsets, cache_lens, bro_r, co_r, w_uk,
                        w_uv, scale, buffers, rows_in_row, mask=MLA_MASK_CAUSAL, workspace=None,
                        status=None, kv_lora_rank=512, stream=None, flags=0):
-    """One buffer row from the paged latent cache: gather its rows, up-project
-    K_nope and V, then the row's attention with the gathered K_rope columns."""
+    """One buffer row from the paged latent cache: K_nope and V projected from
+    the gathered c_kv rows (one launch), then the row's attention with K_rope
+    read from the same cache through the page table."""
     n = int(rows_in_row)
-    rows = buffers.rows[:n]
-    gather_rows(rows, cache, page_table, bro_r, co_r, status, stream)
-    H = q.shape[1]
     kn, v = buffers.k_nope[:n], buffers.v[:n]
-    up_project(kn.view(n, H * 128), rows[:, :kv_lora_rank], w_uk, buffers.gemm_ws, stream)
-    up_project(v.view(n, H * 128), rows[:, :kv_lora_rank], w_uv, buffers.gemm_ws, stream)
-    return prefill_ragged_chunk_contiguous(po, pl, q, kn, v, rows[:, kv_lora_rank:kv_lora_rank + 64],
-                                           row_offsets, cache_lens, bro_r, co_r, scale, mask,
-                                           workspace, stream=stream, flags=flags)
+    gather_up_project(kn, v, cache, w_uk, w_uv, page_table, bro_r, co_r, kv_lora_rank, status, stream)
+    return prefill_ragged_chunk(po, pl, q, kn, v, latent_rope_pages(cache, kv_lora_rank), page_table,
+                                row_offsets, cache_lens, bro_r, co_r, scale, mask, workspace,
+                                stream=stream, flags=flags)
 
 
 def merge(out, partial_out, partial_lse, row_offsets, buffer_row_offsets, stream=None):

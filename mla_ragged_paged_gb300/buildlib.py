@@ -18,7 +18,7 @@ LIB_NAME = "libmla_prefill.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 BUILD_DIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["host_common.cpp", "plan.cu", "attention.cu", "merge.cu", "gather.cu", "upproj.cpp"]
+SOURCES = ["host_common.cpp", "plan.cu", "attention.cu", "merge.cu", "gather.cu", "upproj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
          "-diag-suppress", "177"]
@@ -67,10 +67,7 @@ def build(force=False, verbose=False):
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB_PATH + ".tmp"
-    # cuBLASLt (the up-projection GEMM) is linked dynamically from the toolkit.
-    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-L" + cuda_lib,
-           "-lcublasLt", "-Xlinker", "-rpath," + cuda_lib]
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -272,13 +272,51 @@ def test_up_project_rejects_bad_arguments(lib):
     f = lib.mla_up_project
     bad = binding.MLA_ERR_INVALID_ARG
     out, lat, wt = _desc([8, 256]), _desc([8, 512]), _desc([256, 512])
-    assert f(r(_desc([8, 128])), r(lat), r(wt), None, 0, None) == bad       # N mismatch
-    assert f(r(out), r(_desc([8, 500])), r(wt), None, 0, None) == bad       # K mismatch
-    assert f(r(out), r(lat), r(_desc([256, 512], binding.MLA_DTYPE_F32)), None, 0, None) == bad
-    assert f(r(out), r(lat), r(wt), None, 1024, None) == bad                # workspace NULL
+    assert f(r(_desc([8, 128])), r(lat), r(wt), None, None) == bad       # N mismatch
+    assert f(r(_desc([9, 256])), r(lat), r(wt), None, None) == bad       # rows mismatch
+    assert f(r(out), r(_desc([8, 500])), r(wt), None, None) == bad       # K mismatch
+    assert f(r(out), r(lat), r(_desc([256, 512], binding.MLA_DTYPE_F32)), None, None) == bad
     odd = _desc([8, 512])
-    odd.stride[0] = 516                                                     # 1032-byte rows
-    assert f(r(out), r(odd), r(wt), None, 0, None) == bad
+    odd.stride[0] = 516                                                  # 1032-byte rows
+    assert f(r(out), r(odd), r(wt), None, None) == bad
+    unaligned = _desc([8, 512], ptr=0x10008)
+    assert f(r(out), r(unaligned), r(wt), None, None) == bad
+
+
+@pytest.mark.parametrize("case", ["page_stride", "rank0", "rank_wide", "rank_odd", "v_without_w",
+                                  "w_without_v", "no_bro", "no_co", "table_dtype", "k_rows", "w_k"])
+def test_gather_up_project_rejects_bad_arguments(lib, case):
+    r = lambda d: None if d is None else ctypes.byref(d)
+    k_out, v_out = _desc([100, 256]), _desc([100, 256])
+    cache, pt = _desc([4, 16, 576]), _desc([2, 3], binding.MLA_DTYPE_U32)
+    w_uk, w_uv = _desc([256, 512]), _desc([256, 512])
+    bro, co, rank = 0x60000, 0x70000, 512
+    if case == "page_stride":
+        cache.stride[0] = 16 * 576 + 64          # padded pages: not one row matrix
+    elif case == "rank0":
+        rank = 0
+    elif case == "rank_wide":
+        rank = 584
+    elif case == "rank_odd":
+        rank = 500
+    elif case == "v_without_w":
+        w_uv = None
+    elif case == "w_without_v":
+        v_out = None
+    elif case == "no_bro":
+        bro = None
+    elif case == "no_co":
+        co = None
+    elif case == "table_dtype":
+        pt = _desc([2, 3])
+    elif case == "k_rows":
+        k_out = _desc([100, 128])
+    elif case == "w_k":
+        w_uk = _desc([256, 448])
+    st = lib.mla_gather_up_project(r(k_out), r(v_out), r(cache), r(w_uk), r(w_uv), r(pt), bro, co, rank,
+                                   None, None)
+    assert st == binding.MLA_ERR_INVALID_ARG, case
+    assert lib.mla_last_error_string()
 
 
 @pytest.mark.parametrize("case", ["no_q_rope", "q_nope_192", "q_rope_fp8", "q_rope_shape", "batch_rows",
