@@ -402,13 +402,14 @@ mla_status_t mla_gather_rows(const mla_tensor_t* dst, const mla_tensor_t* cache,
  *   out     device bf16 [rows, N] (e.g. K_nope [rows, H, 128] viewed as
  *           [rows, H * 128]), row stride a multiple of 16 bytes
  *   latent  device bf16 [rows, K] (row stride may exceed K: the c_kv
- *           columns of gathered latent rows)
+ *           columns of gathered latent rows); 1 <= K <= 512 (the latent
+ *           width, kv_lora_rank: a 128-row block of it stays on chip)
  *   weight  device bf16 [N, K] (nn.Linear layout)
  *   status  device uint32 or NULL: MLA_DEVICE_STATUS_TIMEOUT is ORed in if a
  *           pipeline wait of the kernel gives up
  * Rows of every operand must start 16-byte aligned.  One launch of this
  * library's tensor-core GEMM (fp32 accumulation in tensor memory, bf16
- * output, 128 x 256 output tiles); no library GEMM, no workspace.
+ * output, 128 x 128 output tiles); no library GEMM, no workspace.
  */
 mla_status_t mla_up_project(const mla_tensor_t* out, const mla_tensor_t* latent,
                             const mla_tensor_t* weight, uint32_t* status, mla_stream_t stream);
@@ -438,7 +439,8 @@ mla_status_t mla_up_project(const mla_tensor_t* out, const mla_tensor_t* latent,
  *   w_uk, w_uv    device bf16 [N, kv_lora_rank] (nn.Linear layout)
  *   page_table    device uint32 [B, max_pages]
  *   buffer_row_offsets, cache_offsets  one row of the plan ([B+1], [B])
- *   kv_lora_rank  K of the projection, a multiple of 8 (512 for DeepSeek-V3)
+ *   kv_lora_rank  K of the projection, a multiple of 8 and at most 512 (512
+ *                 for DeepSeek-V3)
  *   status        device uint32 or NULL: an out-of-range page id or page-table
  *                 column ORs MLA_DEVICE_STATUS_BAD_PAGE / _BAD_COLUMN, a
  *                 pipeline wait that gives up MLA_DEVICE_STATUS_TIMEOUT

@@ -5,22 +5,33 @@
 // prefill kernel gather K/V entries into a contiguous buffer;
 // mla_prefill_v2_ragged Args: v is the nope segment of the latent cache).
 //   out[t, n] = sum_k A[t, k] * W[n, k]          (W in nn.Linear layout [N, K])
-// A dense bf16 GEMM on the tensor cores: tcgen05.mma with both operands in
-// shared memory, fp32 accumulation in tensor memory, bf16 output.  A is
-// either a plain row-major matrix or, fused with the gather, the first K
-// columns of a buffer row's cache rows, fetched through the page table by TMA
-// row gathers (four rows per instruction) straight into the operand tiles.
+// A dense bf16 GEMM on the tensor cores (tcgen05.mma, fp32 accumulation in
+// tensor memory, bf16 output).  A is either a plain row-major matrix or, fused
+// with the gather, the first K columns of a buffer row's cache rows, fetched
+// through the page table by TMA row gathers (four rows per instruction).
 //
-// Persistent kernel, one CTA of 192 threads per SM, output tiles of 128 x 256:
-//   warp 0     producer: per 64-wide K block one A tile (128 rows) and one B
-//              tile (256 weight rows) by TMA into a 4-stage ring (48 KB each)
-//   warp 1     UMMA issuer (one thread, M128 N256 K16) and tensor-memory owner
+// K is at most 512 (kv_lora_rank), so a 128-row block of A fits in tensor
+// memory (256 columns of packed bf16 pairs) and stays there while the CTA
+// runs through its output tiles of that block: only the weight tiles stream
+// through shared memory, 16 KB per 64-wide K block (64 bytes per tensor-core
+// cycle instead of 96 when both operands stream), and A is fetched (or
+// gathered) once per 128 rows instead of once per output tile.  A ring slot
+// holds two 64-wide K blocks (32 KB), so the one issuing thread waits once
+// per eight UMMAs.
+//
+// Persistent kernel, one CTA of 192 threads per SM; each CTA takes a
+// contiguous range of 128 x 128 output tiles, row block by row block:
+//   warp 0     producer: TMA of A's K blocks when the row block changes, then
+//              per tile its weight K blocks, into a 6-slot ring of 32 KB
+//   warp 1     tensor-core thread and tensor-memory owner: copies A's K blocks
+//              from shared into tensor memory (tcgen05.cp), then per tile 32
+//              UMMAs M128 N128 K16 with A read from tensor memory
 //   warps 2-5  epilogue: tensor memory -> bf16 -> 128B-swizzled staging ->
 //              TMA tile store, 64 columns at a time through two 16 KB buffers
-// Tensor memory holds two 256-column fp32 accumulators, so the epilogue of
-// one tile overlaps the main loop of the next.  With two weight matrices
-// (K_nope and V from the same latent rows) the tiles of both outputs are
-// scheduled in one launch.
+// Tensor memory: A [0, 256), two accumulators [256, 384) and [384, 512), so
+// the epilogue of one tile overlaps the main loop of the next.  With two
+// weight matrices (K_nope and V from the same latent rows) the tiles of both
+// outputs share the resident A.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -35,22 +46,23 @@ namespace mla {
 namespace {
 
 constexpr int kGM = 128;        // output rows per tile (= tensor-memory lanes)
-constexpr int kGN = 256;        // output columns per tile (UMMA N)
-constexpr int kGK = 64;         // K per stage: one 128-byte swizzle atom of bf16
-constexpr int kGStages = 4;
+constexpr int kGN = 128;        // output columns per tile (UMMA N)
+constexpr int kGAtom = 64;      // K per 128-byte swizzle atom of bf16
+constexpr int kGMaxK = 512;     // A block resident in tensor memory: 128 x 512 bf16
+constexpr int kGStages = 6;
 constexpr int kGThreads = 192;
-constexpr uint32_t kGStageA = kGM * kGK * 2;   // 16 KB
-constexpr uint32_t kGStageB = kGN * kGK * 2;   // 32 KB
+constexpr uint32_t kGAtomBytes = 128 * kGAtom * 2;  // 16 KB: 128 rows of one atom
+constexpr uint32_t kGChunk = 2 * kGAtomBytes;       // a ring slot: two atoms
 constexpr uint32_t kGSlab = kGM * 64 * 2;      // 16 KB: 64 output columns of a tile
-constexpr uint32_t kGTmemCols = 2 * kGN;
+constexpr uint32_t kGTmemCols = 512;
+constexpr uint32_t kGColAcc = kGMaxK / 2;      // accumulators after A's 256 columns
 
 struct __align__(1024) GemmSmem {
-  uint8_t a[kGStages][kGStageA];
-  uint8_t b[kGStages][kGStageB];
+  uint8_t ring[kGStages][kGChunk];
   uint8_t c[2][kGSlab];
   uint64_t full[kGStages], empty[kGStages];
   uint64_t acc_full[2], acc_empty[2];
-  uint64_t drain;
+  uint64_t a_drain, drain;
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -58,9 +70,9 @@ static_assert(sizeof(GemmSmem) + 1024 <= 232448, "up-projection shared memory");
 
 struct GemmParams {
   CUtensorMap tm_a;     // contiguous A [M, K], box 64 x 128; or cache rows [slots, K], box 64 x 1
-  CUtensorMap tm_b[2];  // weights [N, K], box 64 x 256
+  CUtensorMap tm_b[2];  // weights [N, K], box 64 x 128
   CUtensorMap tm_c[2];  // outputs [M, N], box 64 x 128
-  uint32_t M, k_blocks, m_tiles, n_tiles, num_out;
+  uint32_t M, k_atoms, m_tiles, n_tiles, num_out;  // k_atoms = ceil(K / 64)
   // Row gather: buffer position t holds context token co[b] + t - bro[b] of
   // the sequence b with bro[b] <= t < bro[b+1]; its cache row (slot) is
   // page_table[b, a / P] * P + a % P.
@@ -73,16 +85,24 @@ struct GemmParams {
   uint32_t* status;
 };
 
+// Tiles in row-block-major order: t = (m * num_out + o) * n_tiles + n.
 struct TileIdx {
   uint32_t m, n, o;
 };
 __device__ __forceinline__ TileIdx tile_of(const GemmParams& p, uint32_t t) {
   TileIdx r;
-  r.m = t % p.m_tiles;
-  const uint32_t rest = t / p.m_tiles;
+  const uint32_t per_m = p.n_tiles * p.num_out;
+  r.m = t / per_m;
+  const uint32_t rest = t - r.m * per_m;
   r.o = rest / p.n_tiles;
   r.n = rest - r.o * p.n_tiles;
   return r;
+}
+// This CTA's contiguous share of the tiles.
+__device__ __forceinline__ void tile_range(const GemmParams& p, uint32_t& t0, uint32_t& t1) {
+  const unsigned long long total = static_cast<unsigned long long>(p.m_tiles) * p.n_tiles * p.num_out;
+  t0 = static_cast<uint32_t>(total * blockIdx.x / gridDim.x);
+  t1 = static_cast<uint32_t>(total * (blockIdx.x + 1) / gridDim.x);
 }
 
 // Cache slot of buffer position t (slot 0 for positions past the row's
@@ -108,36 +128,64 @@ __device__ __forceinline__ int32_t gather_slot(const GemmParams& p, uint32_t t, 
   return static_cast<int32_t>(page * p.P + (a - col * p.P));
 }
 
+// One 128-lane x 256-bit copy from shared memory (an operand descriptor) into
+// tensor memory: 32 bytes of each of 128 rows.  Ordered with the tcgen05.mma
+// instructions the same thread issues afterwards.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 __device__ void gemm_producer(GemmSmem& s, const GemmParams& p, int lane, volatile uint32_t* abort) {
-  const uint32_t total = p.m_tiles * p.n_tiles * p.num_out;
-  uint32_t pos = 0;                 // ring position (K blocks issued)
+  uint32_t t0, t1;
+  tile_range(p, t0, t1);
+  uint32_t pos = 0;                 // ring position (chunks issued)
   uint32_t cur_m = 0xFFFFFFFFu;
-  int32_t rows[4] = {0, 0, 0, 0};   // gather: cache slots of this lane's four tile rows
   uint32_t bad = 0;
   bool alive = true;
-  for (uint32_t t = blockIdx.x; t < total && alive; t += gridDim.x) {
+  // Claim the next ring slot and arm its barrier for `atoms` 16 KB atoms.
+  auto acquire = [&](uint32_t atoms, uint32_t& bar, uint32_t& dst) -> bool {
+    const uint32_t st = pos % kGStages;
+    if (!mbar_wait(smem_u32(&s.empty[st]), ((pos / kGStages) & 1u) ^ 1u, abort)) return false;
+    bar = smem_u32(&s.full[st]);
+    dst = smem_u32(s.ring[st]);
+    if (lane == 0) mbar_arrive_expect_tx(bar, atoms * kGAtomBytes);
+    __syncwarp();
+    ++pos;
+    return true;
+  };
+  for (uint32_t t = t0; t < t1 && alive; ++t) {
     const TileIdx ti = tile_of(p, t);
-    if (p.gather && ti.m != cur_m) {
+    if (ti.m != cur_m) {
+      // A's K blocks of the new row block (gather: rows 4*lane .. 4*lane+3
+      // of each block, 128 bytes each).
       cur_m = ti.m;
+      int32_t rows[4] = {0, 0, 0, 0};
+      if (p.gather) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) rows[j] = gather_slot(p, ti.m * kGM + lane * 4 + j, bad);
+        for (int j = 0; j < 4; ++j) rows[j] = gather_slot(p, ti.m * kGM + lane * 4 + j, bad);
+      }
+      for (uint32_t a0 = 0; a0 < p.k_atoms && alive; a0 += 2) {
+        const uint32_t na = min(2u, p.k_atoms - a0);
+        uint32_t bar, dst;
+        if (!(alive = acquire(na, bar, dst))) break;
+        for (uint32_t a = 0; a < na; ++a) {
+          const int32_t x = static_cast<int32_t>((a0 + a) * kGAtom);
+          if (p.gather) {
+            tma_gather4_2d(dst + a * kGAtomBytes + lane * 512u, &p.tm_a, bar, x, rows[0], rows[1], rows[2], rows[3]);
+          } else if (lane == 0) {
+            tma_load_2d(dst + a * kGAtomBytes, &p.tm_a, bar, x, static_cast<int32_t>(ti.m * kGM));
+          }
+        }
+      }
     }
-    for (uint32_t kb = 0; kb < p.k_blocks; ++kb, ++pos) {
-      const uint32_t st = pos % kGStages;
-      if (!mbar_wait(smem_u32(&s.empty[st]), ((pos / kGStages) & 1u) ^ 1u, abort)) {
-        alive = false;
-        break;
-      }
-      const uint32_t bar = smem_u32(&s.full[st]);
-      const int32_t x = static_cast<int32_t>(kb * kGK);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar, kGStageA + kGStageB);
-        if (!p.gather) tma_load_2d(smem_u32(s.a[st]), &p.tm_a, bar, x, static_cast<int32_t>(ti.m * kGM));
-        tma_load_2d(smem_u32(s.b[st]), &p.tm_b[ti.o], bar, x, static_cast<int32_t>(ti.n * kGN));
-      }
-      __syncwarp();
-      // Rows 4*lane .. 4*lane + 3 of the A tile, 128 bytes each.
-      if (p.gather) tma_gather4_2d(smem_u32(s.a[st]) + lane * 512u, &p.tm_a, bar, x, rows[0], rows[1], rows[2], rows[3]);
+    for (uint32_t a0 = 0; a0 < p.k_atoms && alive; a0 += 2) {
+      const uint32_t na = min(2u, p.k_atoms - a0);
+      uint32_t bar, dst;
+      if (!(alive = acquire(na, bar, dst))) break;
+      if (lane == 0)
+        for (uint32_t a = 0; a < na; ++a)
+          tma_load_2d(dst + a * kGAtomBytes, &p.tm_b[ti.o], bar, static_cast<int32_t>((a0 + a) * kGAtom),
+                      static_cast<int32_t>(ti.n * kGN));
     }
   }
   for (int o = 16; o; o >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o);
@@ -147,52 +195,88 @@ __device__ void gemm_producer(GemmSmem& s, const GemmParams& p, int lane, volati
     const uint32_t n = pos < kGStages ? pos : kGStages;
     for (uint32_t i = 1; i <= n; ++i) {
       const uint32_t q = pos - i;
-      const uint64_t t0 = global_timer_ns();
+      const uint64_t t0n = global_timer_ns();
       while (!mbar_try_wait(smem_u32(&s.full[q % kGStages]), (q / kGStages) & 1u))
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
+        if (global_timer_ns() - t0n > kWaitTimeoutNs) break;
     }
   }
 }
 
 __device__ void gemm_mma(GemmSmem& s, const GemmParams& p, uint32_t tmem, volatile uint32_t* abort) {
-  const uint32_t total = p.m_tiles * p.n_tiles * p.num_out;
+  uint32_t t0, t1;
+  tile_range(p, t0, t1);
   const uint32_t idesc = make_idesc(kGM, kGN, 1, false);  // bf16 A and B, both K-major
-  uint32_t pos = 0, tl = 0;
+  uint32_t pos = 0, tl = 0, drains = 0;
+  uint32_t cur_m = 0xFFFFFFFFu;
   bool alive = true;
-  for (uint32_t t = blockIdx.x; t < total && alive; t += gridDim.x, ++tl) {
-    const uint32_t buf = tl & 1u;
-    if (!mbar_wait(smem_u32(&s.acc_empty[buf]), ((tl >> 1) & 1u) ^ 1u, abort)) break;
+  // Wait for the next ring chunk; returns its shared address.
+  auto next_chunk = [&](uint32_t& addr) -> bool {
+    const uint32_t st = pos % kGStages;
+    if (!mbar_wait(smem_u32(&s.full[st]), (pos / kGStages) & 1u, abort)) return false;
     tc_fence_after();
-    const uint32_t d = tmem + buf * kGN;
-    for (uint32_t kb = 0; kb < p.k_blocks; ++kb, ++pos) {
-      const uint32_t st = pos % kGStages;
-      if (!mbar_wait(smem_u32(&s.full[st]), (pos / kGStages) & 1u, abort)) {
-        alive = false;
-        break;
+    addr = smem_u32(s.ring[st]);
+    return true;
+  };
+  auto release = [&]() {
+    umma_commit(smem_u32(&s.empty[pos % kGStages]));
+    ++pos;
+  };
+  for (uint32_t t = t0; t < t1 && alive; ++t, ++tl) {
+    const TileIdx ti = tile_of(p, t);
+    if (ti.m != cur_m) {
+      if (cur_m != 0xFFFFFFFFu) {
+        // Every UMMA reading the old A must complete before it is overwritten.
+        umma_commit(smem_u32(&s.a_drain));
+        if (!(alive = mbar_wait(smem_u32(&s.a_drain), drains & 1u, abort))) break;
+        ++drains;
+        tc_fence_after();
       }
-      tc_fence_after();
-      const uint64_t ad = sw128_desc_at(smem_u32(s.a[st])), bd = sw128_desc_at(smem_u32(s.b[st]));
+      cur_m = ti.m;
+      for (uint32_t a0 = 0; a0 < p.k_atoms && alive; a0 += 2) {
+        uint32_t a;
+        if (!(alive = next_chunk(a))) break;
+        for (uint32_t at = a0; at < a0 + 2 && at < p.k_atoms; ++at) {
+          const uint64_t ad = sw128_desc_at(a + (at - a0) * kGAtomBytes);
 #pragma unroll
-      for (int k = 0; k < kGK / 16; ++k) umma_f16_ss(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
-      umma_commit(smem_u32(&s.empty[st]));
+          for (int k = 0; k < kGAtom / 16; ++k) tmem_cp_128x256b(tmem + at * 32 + k * 8, ad + 2 * k);
+        }
+        release();
+      }
+      if (!alive) break;
+    }
+    const uint32_t buf = tl & 1u;
+    if (!(alive = mbar_wait(smem_u32(&s.acc_empty[buf]), ((tl >> 1) & 1u) ^ 1u, abort))) break;
+    tc_fence_after();
+    const uint32_t d = tmem + kGColAcc + buf * kGN;
+    for (uint32_t a0 = 0; a0 < p.k_atoms && alive; a0 += 2) {
+      uint32_t b;
+      if (!(alive = next_chunk(b))) break;
+      for (uint32_t at = a0; at < a0 + 2 && at < p.k_atoms; ++at) {
+        const uint64_t bd = sw128_desc_at(b + (at - a0) * kGAtomBytes);
+#pragma unroll
+        for (int k = 0; k < kGAtom / 16; ++k)
+          umma_f16_ts(d, tmem + at * 32 + k * 8, bd + 2 * k, idesc, (at | k) != 0);
+      }
+      release();
     }
     if (alive) umma_commit(smem_u32(&s.acc_full[buf]));
   }
   // No UMMA may still be in flight when tensor memory is released.
   umma_commit(smem_u32(&s.drain));
-  const uint64_t t0 = global_timer_ns();
+  const uint64_t tw = global_timer_ns();
   while (!mbar_try_wait(smem_u32(&s.drain), 0))
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
+    if (global_timer_ns() - tw > kWaitTimeoutNs) break;
 }
 
 __device__ void gemm_epilogue(GemmSmem& s, const GemmParams& p, uint32_t tmem, int quarter, int lane,
                               volatile uint32_t* abort) {
-  const uint32_t total = p.m_tiles * p.n_tiles * p.num_out;
+  uint32_t t0, t1;
+  tile_range(p, t0, t1);
   const int r = quarter * 32 + lane;                     // tile row == tensor-memory lane
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const bool issuer = threadIdx.x == 64;                 // first epilogue thread stores
   uint32_t tl = 0, slab = 0;
-  for (uint32_t t = blockIdx.x; t < total; t += gridDim.x, ++tl) {
+  for (uint32_t t = t0; t < t1; ++t, ++tl) {
     const TileIdx ti = tile_of(p, t);
     const uint32_t buf = tl & 1u;
     if (!mbar_wait(smem_u32(&s.acc_full[buf]), (tl >> 1) & 1u, abort)) break;
@@ -200,7 +284,7 @@ __device__ void gemm_epilogue(GemmSmem& s, const GemmParams& p, uint32_t tmem, i
 #pragma unroll 1
     for (int c = 0; c < kGN / 64; ++c, ++slab) {
       uint32_t v0[32], v1[32];
-      const uint32_t col = tmem + lane_off + buf * kGN + c * 64;
+      const uint32_t col = tmem + lane_off + kGColAcc + buf * kGN + c * 64;
       tmem_ld_32x32b_x32(col, v0);
       tmem_ld_32x32b_x32(col + 32, v1);
       tmem_ld_wait();
@@ -254,6 +338,7 @@ __global__ void __launch_bounds__(kGThreads, 1) up_project_kernel(const __grid_c
       mbar_init(smem_u32(&s.acc_full[i]), 1);
       mbar_init(smem_u32(&s.acc_empty[i]), 4);  // the four epilogue warps
     }
+    mbar_init(smem_u32(&s.a_drain), 1);
     mbar_init(smem_u32(&s.drain), 1);
     fence_barrier_init();
   }
@@ -312,6 +397,8 @@ mla_status_t encode_matrix(CUtensorMap* map, const mla_tensor_t* t, uint64_t col
 mla_status_t setup_outputs(GemmParams& p, const mla_tensor_t* const* outs, const mla_tensor_t* const* weights,
                            uint32_t num_out, int64_t M, int64_t K) {
   mla_status_t st;
+  if (K > kGMaxK) return fail(MLA_ERR_INVALID_ARG, "K = %lld exceeds %d (the latent width the kernel keeps on chip)",
+                              (long long)K, kGMaxK);
   int64_t N = -1;
   for (uint32_t o = 0; o < num_out; ++o) {
     if ((st = check_matrix(outs[o], o ? "v_out" : "out")) != MLA_OK) return st;
@@ -326,7 +413,7 @@ mla_status_t setup_outputs(GemmParams& p, const mla_tensor_t* const* outs, const
   }
   if (N < 1 || K < 1) return fail(MLA_ERR_INVALID_ARG, "empty projection");
   p.M = static_cast<uint32_t>(M);
-  p.k_blocks = static_cast<uint32_t>((K + kGK - 1) / kGK);
+  p.k_atoms = static_cast<uint32_t>((K + kGAtom - 1) / kGAtom);
   p.m_tiles = static_cast<uint32_t>((M + kGM - 1) / kGM);
   p.n_tiles = static_cast<uint32_t>((N + kGN - 1) / kGN);
   p.num_out = num_out;

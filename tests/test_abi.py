@@ -281,6 +281,7 @@ def test_up_project_rejects_bad_arguments(lib):
     assert f(r(out), r(odd), r(wt), None, None) == bad
     unaligned = _desc([8, 512], ptr=0x10008)
     assert f(r(out), r(unaligned), r(wt), None, None) == bad
+    assert f(r(out), r(_desc([8, 520])), r(_desc([256, 520])), None, None) == bad   # K above 512
 
 
 @pytest.mark.parametrize("case", ["page_stride", "rank0", "rank_wide", "rank_odd", "v_without_w",
