@@ -476,6 +476,16 @@ mla_status_t mla_read_device_status(const void* workspace, uint32_t* status_out,
  */
 mla_status_t mla_test_inject_stall(uint32_t enable);
 
+/*
+ * Test hook for the pipeline's ordering (no counterpart on the pages).  While
+ * nonzero (process-wide), the softmax warps of the second query tile of every
+ * attention work item wait `nanoseconds` (at most 100000) before loading each
+ * score tile, so that tile runs far behind the first one; results must be
+ * bit-identical to an undelayed launch, only slower.  0 turns it off.  Never
+ * set it outside tests.
+ */
+mla_status_t mla_test_delay_softmax(uint32_t nanoseconds);
+
 /* Text for the last error returned to the calling thread (never NULL). */
 const char* mla_last_error_string(void);
 

@@ -25,7 +25,7 @@ EXPORTS = ["mla_prefill_plan", "mla_prefill_plan_max_rows", "mla_prefill_ragged_
            "mla_prefill_ragged_chunk", "mla_prefill_merge", "mla_prefill_ragged_contiguous",
            "mla_prefill_ragged_chunk_contiguous", "mla_gather_rows", "mla_up_project",
            "mla_gather_up_project",
-           "mla_prefill_ragged_split", "mla_test_inject_stall",
+           "mla_prefill_ragged_split", "mla_test_inject_stall", "mla_test_delay_softmax",
            "mla_read_device_status",
            "mla_last_error_string"]
 
@@ -86,6 +86,8 @@ def load(path=LIB_PATH):
     lib.mla_prefill_ragged_split.restype = ctypes.c_int
     lib.mla_test_inject_stall.argtypes = [u32]
     lib.mla_test_inject_stall.restype = ctypes.c_int
+    lib.mla_test_delay_softmax.argtypes = [u32]
+    lib.mla_test_delay_softmax.restype = ctypes.c_int
     lib.mla_gather_rows.argtypes = [pt, pt, pt, vp, vp, vp, vp]
     lib.mla_gather_rows.restype = ctypes.c_int
     lib.mla_up_project.argtypes = [pt, pt, pt, vp, vp]
@@ -511,6 +513,12 @@ def test_inject_stall(enable):
     """mla_test_inject_stall: make attention launches run into their wait
     timeout (tests of the timeout path only)."""
     _check(load().mla_test_inject_stall(1 if enable else 0))
+
+
+def test_delay_softmax(nanoseconds):
+    """mla_test_delay_softmax: delay the second query tile's softmax before
+    every score-tile load (tests of the pipeline's ordering only)."""
+    _check(load().mla_test_delay_softmax(int(nanoseconds)))
 
 
 def device_status(workspace, stream=None):

@@ -127,6 +127,10 @@ struct AttnParams {
   // Tests of the timeout path only: the producer leaves the first K group of
   // its first work item unloaded, so the UMMA issuers' wait for it runs out.
   uint32_t test_stall;
+  // Tests of the pipeline's ordering only: query tile 1's softmax waits this
+  // many nanoseconds before loading each score tile, so it runs well behind
+  // tile 0 (results must not change).
+  uint32_t test_delay_ns;
   uint32_t H, causal;
   float sl2;
   uint8_t* ws;
@@ -156,7 +160,12 @@ struct __align__(1024) Smem {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[Cfg<FP8>::kRing], kv_empty[Cfg<FP8>::kRing];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
-  uint64_t s_free[2];   // softmax q has loaded its S tile: the S region may be reused
+  // Softmax q has loaded its k-th S tile (barrier [q][k & 1], phase k >> 1):
+  // the S region may be reused.  Two barriers per query tile, taken in turn,
+  // because an issuer may skip one of the other tile's phases (see
+  // mma_thread); with parity waits on a single barrier that skip could match
+  // a phase two behind.
+  uint64_t s_free[2][2];
   uint64_t pv_done[2];  // P_q . V of the previous tile has completed: P_q and O_q are free
   uint64_t drain[2];
   // Per-token K scales: the 128 scales of the KV tile each softmax warpgroup
@@ -904,9 +913,16 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
   constexpr int kV = C::kCPT - kK;
 
   // Wait until the k-th S tile of query tile t has been loaded by its softmax.
+  // The waits of one issuer on tile t's loads are not always consecutive: at
+  // the end of a causal item query tile 1 usually has one more KV tile than
+  // tile 0, so its last two score tiles follow each other in the S region,
+  // and the next item's S0(0) waits for the second of them although issuer 0
+  // never waited for the first.  The other tile's load count is then one or
+  // two ahead of issuer 0's last wait; barrier [t][k & 1] with phase k >> 1
+  // tells those cases apart, where one barrier's parity would not.
   auto wait_region = [&](int t, uint32_t k) -> bool {
     if (t < 0) return true;
-    if (!mbar_wait(smem_u32(&s.s_free[t]), k & 1u, abort)) return false;
+    if (!mbar_wait(smem_u32(&s.s_free[t][k & 1u]), (k >> 1) & 1u, abort)) return false;
     tc_fence_after();
     return true;
   };
@@ -1055,6 +1071,11 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
         if (j + 1 < nkv) ks_next = key_scale(it, j + 1);
       }
       if (!mbar_wait(smem_u32(&s.s_full[q]), sf & 1u, abort)) return;
+      if (q == 1 && p.test_delay_ns) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < p.test_delay_ns) {
+        }
+      }
       ++sf;
       tc_fence_after();
       uint32_t sr[4][32];
@@ -1064,7 +1085,7 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
       // The S region is free for the next score tile.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s.s_free[q]));
+      if (lane == 0) mbar_arrive(smem_u32(&s.s_free[q][(sf - 1) & 1u]));
       // Exponent reference so far (0 before the first visible key).
       float mb = m_used == -INFINITY ? 0.f : m_used;
       if (KTOK) {
@@ -1304,7 +1325,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
       mbar_init(smem_u32(&s.p_full[i]), 4);
       mbar_init(smem_u32(&s.o_full[i]), 1);
       mbar_init(smem_u32(&s.o_empty[i]), 4);
-      mbar_init(smem_u32(&s.s_free[i]), 4);   // the 4 softmax warps of query tile i
+      mbar_init(smem_u32(&s.s_free[i][0]), 4);   // the 4 softmax warps of query tile i
+      mbar_init(smem_u32(&s.s_free[i][1]), 4);
       mbar_init(smem_u32(&s.pv_done[i]), 1);
       mbar_init(smem_u32(&s.ks_full[i]), 4);
       mbar_init(smem_u32(&s.ks_free[i]), 4);
@@ -1428,6 +1450,7 @@ mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t*
 }
 
 std::atomic<uint32_t> g_test_stall{0};
+std::atomic<uint32_t> g_test_delay_ns{0};
 
 // Full-context call (buffer_row_offsets == NULL) or one buffer row of a
 // chunked call (with lse).
@@ -1640,6 +1663,7 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   prm.H = static_cast<uint32_t>(H);
   prm.causal = mask == MLA_MASK_CAUSAL;
   prm.test_stall = g_test_stall.load(std::memory_order_relaxed);
+  prm.test_delay_ns = g_test_delay_ns.load(std::memory_order_relaxed);
   prm.sl2 = scale * 1.4426950408889634f;
   prm.ws = static_cast<uint8_t*>(workspace);
   prm.q_base = static_cast<const uint8_t*>(q->data);
@@ -1705,6 +1729,12 @@ extern "C" mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_te
 
 extern "C" mla_status_t mla_test_inject_stall(uint32_t enable) {
   mla::g_test_stall.store(enable ? 1u : 0u, std::memory_order_relaxed);
+  return MLA_OK;
+}
+
+extern "C" mla_status_t mla_test_delay_softmax(uint32_t nanoseconds) {
+  if (nanoseconds > 100000u) return mla::fail(MLA_ERR_INVALID_ARG, "delay above 100 us");
+  mla::g_test_delay_ns.store(nanoseconds, std::memory_order_relaxed);
   return MLA_OK;
 }
 
