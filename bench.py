@@ -13,9 +13,11 @@ batch (weak scaling, no data-path collective); the step time is the maximum
 over ranks.
 
 --mode chunked times chunked execution instead of the full-context call: the
-plan, one mla_prefill_ragged_chunk per buffer row of buffer_token_size tokens
-(the K buffer of row r being rows r*T .. r*T+T-1 of the batch-order packed
-K/V), then mla_prefill_merge.  Same metric, same work.
+plan, then all its buffer rows of buffer_token_size tokens in one
+mla_prefill_ragged_chunked call (the K buffer of row r being rows
+r*T .. r*T+T-1 of the batch-order packed K/V); --combine fold / merge time one
+mla_prefill_ragged_chunk per row instead, folded in place or followed by
+mla_prefill_merge.  Same metric, same work.
 
 --mode contiguous times mla_prefill_ragged_contiguous: the same K_rope rows laid
 out contiguously (row = K row) instead of paged.
@@ -285,8 +287,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=[c.name for c in workloads.CONFIGS],
                     help="workload to time (default: the DeepSeek-V3-shaped bf16 batch)")
-    ap.add_argument("--combine", default="fold", choices=["fold", "merge"],
-                    help="chunked / latent modes: fold every row into the output in place "
+    ap.add_argument("--combine", default=None, choices=["single", "fold", "merge"],
+                    help="chunked mode: all buffer rows in one mla_prefill_ragged_chunked call (default); "
+                         "chunked / latent modes: one call per row, folding every row into the output in place "
                          "(MLA_CHUNK_ACCUMULATE), or write per-row outputs and run mla_prefill_merge")
     ap.add_argument("--mode", default="full", choices=["full", "chunked", "contiguous", "latent", "split"],
                     help="full-context attention call (paged K_rope); one call per plan buffer row "
@@ -370,8 +373,12 @@ def main():
                 torch.empty((1,), dtype=torch.int32, device=dev))
     stream = torch.cuda.current_stream(dev)
     chunked = args.mode in ("chunked", "latent")
-    fold = chunked and args.combine == "fold"
-    scratch = binding.chunked_scratch(R, Tq, H, dev) if chunked and not fold else None
+    combine = args.combine or ("single" if args.mode == "chunked" else "fold")
+    if latent and combine == "single":
+        ap.error("--combine single applies to --mode chunked")
+    single = chunked and combine == "single"
+    fold = chunked and combine == "fold"
+    scratch = binding.chunked_scratch(R, Tq, H, dev) if chunked and combine == "merge" else None
     lse_buf = torch.empty((Tq, H), dtype=torch.float32, device=dev) if fold else None
     lbuf = binding.LatentRowBuffers(T, H, dev) if latent else None
 
@@ -394,6 +401,14 @@ def main():
             binding.prefill_ragged(o, inp["q"], inp["k_nope"], inp["v"], inp["k_rope_pool"],
                                    inp["page_table"], inp["row_offsets"], inp["cache_lens"], w.scale,
                                    binding.MLA_MASK_CAUSAL, ws, stream=stream, **scales)
+            return
+        if single:
+            # Every buffer row of the plan in one call; the rows' K buffers
+            # are the packed K/V, stacked T rows apart.
+            binding.prefill_ragged_chunked(o, inp["q"], inp["k_nope"], inp["v"], inp["k_rope_pool"],
+                                           inp["page_table"], inp["row_offsets"], inp["cache_lens"],
+                                           plan_out[0], plan_out[1], plan_out[3], T, w.scale,
+                                           binding.MLA_MASK_CAUSAL, ws, stream=stream, **scales)
             return
         flags = binding.MLA_CHUNK_ACCUMULATE if fold else 0
         for r in range(R):
@@ -421,7 +436,7 @@ def main():
                                          inp["cache_lens"], plan_out[0][r], plan_out[1][r], w.scale,
                                          binding.MLA_MASK_CAUSAL, ws, stream=stream, flags=flags,
                                          **row_scales)
-        if not fold:
+        if combine == "merge":
             tick("merge")
             binding.merge(o, scratch[0], scratch[1], inp["row_offsets"], plan_out[0], stream=stream)
 
@@ -533,7 +548,7 @@ def main():
     if ATTENTION_TRAFFIC["source_sha1"] == source_sha1() and args.mode == "full":
         traffic = ATTENTION_TRAFFIC["bytes_per_launch"].get(spec.name + (" per-token K" if ktok else ""))
     merge_roofline = None
-    if chunked and not fold:
+    if combine == "merge" and chunked:
         # Algorithmic merge bytes: per (token, head), 256 + 4 bytes read from
         # each row holding keys of its sequence, 256 bytes written.
         G = np.concatenate([[0], np.cumsum(w.n + w.prior)])
@@ -565,16 +580,16 @@ def main():
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
                "sample": sample + f"; {dt:.1f} s of float64 numpy on the host"}
 
-    # This library's kernels per step (cuBLASLt's GEMM kernels not counted).
+    # This library's kernels per step.
     if latent:
         launches_per_step = 1 + 3 * R          # plan; per row gather + up-projection, scheduler, attention
-    elif chunked:
+    elif chunked and not single:
         launches_per_step = 1 + R * (3 if fp8 else 2)
     else:
-        launches_per_step = 4 if fp8 else 3
-    if chunked and not fold:
+        launches_per_step = 4 if fp8 else 3    # plan, scheduler, (fp8: K_rope conversion), attention
+    if chunked and combine == "merge":
         launches_per_step += 1                 # merge
-    merge_txt = "" if fold else " + mla_prefill_merge"
+    merge_txt = " + mla_prefill_merge" if combine == "merge" else ""
     if rank == 0:
         value = F_all * args.steps / (total_ms * 1e-3) / 1e12
         line = {
@@ -589,6 +604,8 @@ def main():
                        "step": ("mla_prefill_plan + %d x (mla_gather_up_project + "
                                 "mla_prefill_ragged_chunk, K_rope from the latent cache) (T=%d)%s" % (R, T, merge_txt))
                                if latent else
+                               ("mla_prefill_plan + mla_prefill_ragged_chunked over its %d rows (T=%d)" % (R, T))
+                               if single else
                                ("mla_prefill_plan + %d x mla_prefill_ragged_chunk (T=%d)%s"
                                 % (R, T, merge_txt)) if chunked else
                                ("mla_prefill_plan + mla_prefill_ragged_contiguous (K_rope [S_k, 64], not paged)"
@@ -603,7 +620,8 @@ def main():
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                          "kernel": ("mla_attention_kernel over %d buffer rows (+ their scheduler launches)" % R)
-                                   if chunked else "mla_attention_kernel (+ its 1-CTA scheduler launch in the span)",
+                                   if chunked and not single else
+                                   "mla_attention_kernel (+ its 1-CTA scheduler launch in the span)",
                          "peak_source": f"{peak_src} bf16_tflops (burst)" + (" x 2 (fp8/bf16 nominal ratio)" if fp8 else "")},
             "cpu_baseline": cpu,
         }
@@ -611,7 +629,9 @@ def main():
             line["config"]["k_scales"] = ("one K_nope scale per K row (re-quantised per row)" if ktok
                                           else "per-tensor K_nope scale")
         if chunked:
-            line["config"]["combine"] = "in-place fold (MLA_CHUNK_ACCUMULATE)" if fold else "mla_prefill_merge"
+            line["config"]["combine"] = {"single": "all rows in one mla_prefill_ragged_chunked call",
+                                         "fold": "one call per row, in-place fold (MLA_CHUNK_ACCUMULATE)",
+                                         "merge": "one call per row + mla_prefill_merge"}[combine]
         if merge_roofline is not None:
             line["roofline_merge"] = merge_roofline
         if latent:

@@ -8,8 +8,9 @@
  *   mla_prefill_ragged  ragged causal attention with a 192-wide Q head, 128
  *                       per-head K_nope dims plus 64 K_rope dims shared by all
  *                       heads, 128-wide V and output (flare_mla_prefill).
- * Chunked execution runs the second stage once per buffer row of the plan
- * (mla_prefill_ragged_chunk) and combines the rows (mla_prefill_merge).
+ * Chunked execution runs the second stage over the plan's buffer rows: all
+ * rows in one call (mla_prefill_ragged_chunked), or one row per call
+ * (mla_prefill_ragged_chunk) folded in place or combined by mla_prefill_merge.
  *
  * Conventions shared by every entry point:
  *   - Every pointer marked "device" is caller-owned device memory; the library
@@ -327,6 +328,49 @@ mla_status_t mla_prefill_ragged_chunk(const mla_tensor_t* out, const mla_tensor_
                                       mla_stream_t stream);
 
 #define MLA_CHUNK_ACCUMULATE 0x1u /* mla_prefill_ragged_chunk*: fold into out / lse */
+
+/*
+ * Chunked execution of every buffer row of the plan in one call and one
+ * attention launch (flare_mla_prefill: Args cache_row_offsets, cache_offsets;
+ * generic_flare_mla_prefill_ragged_paged_plan: Args buffer_row_offsets,
+ * cache_offsets, buffer_lengths; the rows' combination is the log-sum-exp
+ * fold of mla_prefill_ragged_chunk with MLA_CHUNK_ACCUMULATE).
+ *
+ * The rows' K buffers are stacked: row r's buffer is K rows
+ * [r * T, (r + 1) * T) of k_nope / v (T = buffer_token_size), laid out as the
+ * plan describes (sequence b's keys of row r at row-local positions
+ * buffer_row_offsets[r, b] .. [r, b+1]).  Under the plan's global packing a
+ * sequence's windows in consecutive rows are then adjacent K rows, so one work
+ * item covers a (sequence, head, query block) across all its rows and folds
+ * them in its online softmax; the rows share one launch and one tail.  The
+ * result is that of mla_prefill_ragged_chunk applied to rows 0..R-1 in order
+ * with MLA_CHUNK_ACCUMULATE:
+ *   out   the softmax over all the sequence's visible keys (the full-context
+ *         result), bf16 [Tq, H, 128] (written)
+ *   lse   float32 [Tq, H] (written) or NULL: ln sum_j exp(s_j) over the same
+ *         keys
+ *   buffer_row_offsets  device uint32 [max_rows, B+1], cache_offsets device
+ *         uint32 [max_rows, B]: the plan's outputs for these lengths and T
+ *   num_rows            device uint32 [1]: the plan's row count R; rows
+ *         r >= min(R, max_rows) are not read
+ *   k_nope, v           device [>= R * T, H, 128] (fp8 per-token K_nope
+ *         scales: [rows] floats indexed by stacked K row)
+ * Per sequence the kernel checks the first and the last row holding its keys
+ * against the stacked layout (offset, context position and window end); a
+ * sequence whose rows disagree, or that needs a row >= min(R, max_rows), is
+ * skipped and sets MLA_DEVICE_STATUS_BAD_OFFSETS.  Everything else (K_rope,
+ * page table, scales, workspace sizes, masks, errors) as mla_prefill_ragged;
+ * the launches are those of mla_prefill_ragged.
+ */
+mla_status_t mla_prefill_ragged_chunked(const mla_tensor_t* out, const mla_tensor_t* lse,
+                                        const mla_tensor_t* q, const mla_tensor_t* k_nope,
+                                        const mla_tensor_t* v, const mla_tensor_t* k_rope_pages,
+                                        const mla_tensor_t* page_table, const uint32_t* row_offsets,
+                                        const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
+                                        const uint32_t* cache_offsets, const uint32_t* num_rows,
+                                        uint32_t max_rows, uint32_t buffer_token_size, float scale,
+                                        mla_mask_t mask, void* workspace, size_t workspace_bytes,
+                                        mla_stream_t stream);
 
 /*
  * Combines the rows of a chunked execution (the pages give only the per-row

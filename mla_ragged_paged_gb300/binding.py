@@ -22,7 +22,8 @@ STATUS_BITS = {0x1: "BAD_PAGE", 0x2: "BAD_COLUMN", 0x4: "BAD_OFFSETS", 0x8: "TIM
 # Names exported by the C ABI (kept in step with include/mla_prefill.h).
 EXPORTS = ["mla_prefill_plan", "mla_prefill_plan_max_rows", "mla_prefill_ragged_workspace_size",
            "mla_prefill_ragged_workspace_size_fp8", "mla_prefill_ragged", "mla_prefill_ragged_noalloc",
-           "mla_prefill_ragged_chunk", "mla_prefill_merge", "mla_prefill_ragged_contiguous",
+           "mla_prefill_ragged_chunk", "mla_prefill_ragged_chunked", "mla_prefill_merge",
+           "mla_prefill_ragged_contiguous",
            "mla_prefill_ragged_chunk_contiguous", "mla_gather_rows", "mla_up_project",
            "mla_gather_up_project",
            "mla_prefill_ragged_split", "mla_test_inject_stall", "mla_test_delay_softmax",
@@ -72,6 +73,9 @@ def load(path=LIB_PATH):
     lib.mla_prefill_ragged_chunk.argtypes = [pt, pt, pt, pt, pt, pt, pt, vp, vp, vp, vp, ctypes.c_float,
                                              ctypes.c_int, u32, vp, ctypes.c_size_t, vp]
     lib.mla_prefill_ragged_chunk.restype = ctypes.c_int
+    lib.mla_prefill_ragged_chunked.argtypes = [pt, pt, pt, pt, pt, pt, pt, vp, vp, vp, vp, vp, u32, u32,
+                                               ctypes.c_float, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.mla_prefill_ragged_chunked.restype = ctypes.c_int
     lib.mla_prefill_merge.argtypes = [pt, pt, pt, vp, vp, u32, vp]
     lib.mla_prefill_merge.restype = ctypes.c_int
     lib.mla_prefill_ragged_contiguous.argtypes = [pt, pt, pt, pt, pt, vp, vp, u32, ctypes.c_float,
@@ -445,48 +449,50 @@ def chunked_scratch(num_rows, total_q, heads, device="cuda"):
             torch.empty((num_rows, total_q, heads), dtype=torch.float32, device=device))
 
 
-def prefill_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens, scale,
-                    buffer_token_size, total_k, mask=MLA_MASK_CAUSAL, workspace=None, scratch=None,
-                    q_scale=None, k_scale=None, v_scale=None, k_rope_scales=None, stream=None,
-                    fold=False, lse=None):
-    """Chunked execution: the plan, one mla_prefill_ragged_chunk per buffer
-    row, then mla_prefill_merge (or, with fold=True, every row folded into out
-    and lse in place, lse a float32 [Tq, H] tensor or allocated here).  k_nope
-    / v hold the contexts packed in batch order (the full-context layout), so
-    buffer row r's K buffer is rows r*T .. r*T + T - 1 of them.  total_k (host
-    int) is the number of context tokens, sum of (new + cached) lengths, which
-    fixes the row count."""
-    T = int(buffer_token_size)
-    R = max(1, -(-int(total_k) // T))
+def prefill_ragged_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,
+                           buffer_row_offsets, cache_offsets, num_rows, buffer_token_size, scale,
+                           mask=MLA_MASK_CAUSAL, workspace=None, lse=None, q_scale=None, k_scale=None,
+                           v_scale=None, k_rope_scales=None, stream=None):
+    """mla_prefill_ragged_chunked: every buffer row of the plan in one call.
+    buffer_row_offsets [max_rows, B+1] / cache_offsets [max_rows, B] / num_rows
+    [1] are the plan's device outputs; k_nope / v hold the rows' K buffers
+    stacked buffer_token_size rows apart."""
+    lib = load()
     B = page_table.shape[0]
     fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
     if workspace is None:
-        slots = k_rope_pages.shape[0] * k_rope_pages.shape[1] if fp8 else None
-        slots = max(slots, min(T, k_nope.shape[0])) if _per_token(k_scale) else slots
+        slots = _rope_rows(k_nope, k_scale, k_rope_pages.shape[0] * k_rope_pages.shape[1]) if fp8 else None
         workspace = alloc_workspace(B, q.device, slots)
-    bro, co, _, _ = plan(row_offsets, cache_lens, T, R, stream=stream)
-    Sk = k_nope.shape[0]
-    # Per-token K scales follow their rows into each buffer row's slice.
-    ks = (lambda lo, hi: k_scale[lo:hi]) if _per_token(k_scale) else (lambda lo, hi: k_scale)
-    if fold:
-        if lse is None:
-            lse = torch.empty((q.shape[0], q.shape[1]), dtype=torch.float32, device=q.device)
-        for r in range(R):
-            lo, hi = r * T, min((r + 1) * T, Sk)
-            prefill_ragged_chunk(out, lse, q, k_nope[lo:hi], v[lo:hi], k_rope_pages, page_table,
-                                 row_offsets, cache_lens, bro[r], co[r], scale, mask, workspace,
-                                 q_scale, ks(lo, hi), v_scale, k_rope_scales, stream,
-                                 flags=MLA_CHUNK_ACCUMULATE)
-        return out
-    if scratch is None:
-        scratch = chunked_scratch(R, q.shape[0], q.shape[1], q.device)
-    po, pl = scratch
-    for r in range(R):
-        lo, hi = r * T, min((r + 1) * T, Sk)
-        prefill_ragged_chunk(po[r], pl[r], q, k_nope[lo:hi], v[lo:hi], k_rope_pages, page_table,
-                             row_offsets, cache_lens, bro[r], co[r], scale, mask, workspace,
-                             q_scale, ks(lo, hi), v_scale, k_rope_scales, stream)
-    return merge(out, po[:R], pl[:R], row_offsets, bro, stream)
+    if buffer_row_offsets.dim() != 2 or buffer_row_offsets.shape[1] != B + 1 or \
+            buffer_row_offsets.stride(0) != B + 1 or cache_offsets.dim() != 2 or \
+            cache_offsets.shape != (buffer_row_offsets.shape[0], B) or cache_offsets.stride(0) != B:
+        raise MlaError(MLA_ERR_INVALID_ARG, "plan arrays must be packed [max_rows, B+1] and [max_rows, B]")
+    d_q, d_k, d_v, d_r, d_pt = _inputs(q, k_nope, v, k_rope_pages, page_table, q_scale, k_scale,
+                                       v_scale, k_rope_scales)
+    d_out = describe(out, MLA_DTYPE_BF16)
+    d_lse = describe(lse, MLA_DTYPE_F32) if lse is not None else None
+    _check(lib.mla_prefill_ragged_chunked(ctypes.byref(d_out), ctypes.byref(d_lse) if d_lse is not None else None,
+                                          ctypes.byref(d_q), ctypes.byref(d_k), ctypes.byref(d_v),
+                                          ctypes.byref(d_r), ctypes.byref(d_pt), _ptr(row_offsets),
+                                          _ptr(cache_lens), _ptr(buffer_row_offsets), _ptr(cache_offsets),
+                                          _ptr(num_rows), int(buffer_row_offsets.shape[0]),
+                                          int(buffer_token_size), float(scale), int(mask), _ptr(workspace),
+                                          workspace.numel(), _stream(stream)))
+    return out
+
+
+def prefill_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens, scale,
+                    buffer_token_size, max_rows, mask=MLA_MASK_CAUSAL, workspace=None, q_scale=None,
+                    k_scale=None, v_scale=None, k_rope_scales=None, stream=None, lse=None, plan_out=None):
+    """Chunked execution: mla_prefill_plan, then mla_prefill_ragged_chunked over
+    all its rows.  k_nope / v hold the contexts packed in batch order, i.e. the
+    rows' K buffers stacked buffer_token_size rows apart; max_rows (host int)
+    is the plan's capacity, at least ceil(total context / buffer_token_size)."""
+    bro, co, _, nrows = plan(row_offsets, cache_lens, buffer_token_size, max_rows, stream=stream,
+                             out=plan_out)
+    return prefill_ragged_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,
+                                  bro, co, nrows, buffer_token_size, scale, mask, workspace, lse, q_scale,
+                                  k_scale, v_scale, k_rope_scales, stream)
 
 
 def prefill_ragged_noalloc(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,

@@ -197,6 +197,14 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
 // block from last (most keys) to first, then head.
 constexpr int kSchedThreads = 1024;
 
+// Chunked execution of all buffer rows in one launch (T != 0): the plan's
+// arrays bro [max_rows, B+1] and cof [max_rows, B], R = min(*num_rows,
+// max_rows) rows used, each row's K buffer T rows after the previous one.
+struct StackedRows {
+  const uint32_t* num_rows;
+  uint32_t max_rows, T;
+};
+
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* warp_tot, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = x;
@@ -228,7 +236,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
 schedule_kernel(const uint32_t* __restrict__ ro, const uint32_t* __restrict__ cl,
                 const uint32_t* __restrict__ bro, const uint32_t* __restrict__ cof, uint32_t B,
                 uint32_t H, uint32_t Tq, uint32_t Sk, uint32_t P, uint32_t max_pages,
-                uint32_t kv_bytes_per_key_head, uint8_t* __restrict__ ws) {
+                uint32_t kv_bytes_per_key_head, StackedRows stk, uint8_t* __restrict__ ws) {
   extern __shared__ uint32_t sm[];
   uint32_t* kv_start = sm;           // [B]
   uint32_t* key = sm + B;            // [B]  keys in the window (0 = no work)
@@ -260,7 +268,24 @@ schedule_kernel(const uint32_t* __restrict__ ro, const uint32_t* __restrict__ cl
     // buffer row's W keys from context position co at rows bro[b]...
     uint64_t w0 = 0, W = L, start = run;
     bool ok = hi >= lo && hi <= Tq && L <= 0x7FFFFFFFull;
-    if (bro) {
+    if (stk.T) {
+      // All buffer rows at once, their K buffers stacked T rows apart: the
+      // sequence's context sits at plan rows r0..r1, whose windows are then
+      // adjacent K rows run.. run + L - 1.  Check the first and the last of
+      // those rows against the plan (global packing).
+      ok = ok && static_cast<uint64_t>(run) + L <= Sk;
+      if (ok && L > 0) {
+        const uint32_t R = min(*stk.num_rows, stk.max_rows);
+        const uint64_t g = run, T = stk.T, r0 = g / T, r1 = (g + L - 1) / T;
+        ok = r1 < R;
+        if (ok) {
+          const uint32_t* b0r = bro + r0 * (B + 1);
+          const uint32_t* b1r = bro + r1 * (B + 1);
+          ok = b0r[b] == g - r0 * T && cof[r0 * B + b] == 0 && b1r[b + 1] == g + L - r1 * T &&
+               cof[r1 * B + b] == (r1 == r0 ? 0 : r1 * T - g);
+        }
+      }
+    } else if (bro) {
       const uint32_t r0 = bro[b], r1 = bro[b + 1];
       ok = ok && r0 <= r1 && r1 <= Sk;
       w0 = cof[b];
@@ -318,7 +343,7 @@ schedule_kernel(const uint32_t* __restrict__ ro, const uint32_t* __restrict__ cl
     r.prior = cl[b];
     r.kv_start = kv_start[b];
     r.W = key[b];
-    r.co = bro ? cof[b] : 0u;
+    r.co = bro && !stk.T ? cof[b] : 0u;
     const uint64_t head_bytes = static_cast<uint64_t>(key[b]) * kv_bytes_per_key_head;
     uint64_t g = head_bytes ? kL2GroupBytes / head_bytes : H;
     if (g > H) g = H;
@@ -1404,7 +1429,7 @@ mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t*
                               const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
                               const uint32_t* cache_offsets, uint32_t B, uint32_t H, uint32_t Tq,
                               uint32_t Sk, uint32_t P, uint32_t max_pages, void* workspace,
-                              const RopeRows* rows, cudaStream_t cs) {
+                              const RopeRows* rows, const StackedRows& stk, cudaStream_t cs) {
   mla_status_t st;
   auto* kernel = mla_attention_kernel<FP8, KTOK>;
   {
@@ -1432,7 +1457,7 @@ mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t*
   const uint32_t elt = FP8 ? 1u : 2u;
   schedule_kernel<<<1, kSchedThreads, sched_smem, cs>>>(row_offsets, cache_lens, buffer_row_offsets,
                                                         cache_offsets, B, H, Tq, Sk, P, max_pages,
-                                                        elt * (128 + 128), static_cast<uint8_t*>(workspace));
+                                                        elt * (128 + 128), stk, static_cast<uint8_t*>(workspace));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "scheduler launch: %s", cudaGetErrorString(e));
   if (rows) {
@@ -1462,9 +1487,11 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
                      const mla_tensor_t* page_table, uint32_t contig_batch, const uint32_t* row_offsets,
                      const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
                      const uint32_t* cache_offsets, float scale, mla_mask_t mask, uint32_t flags,
-                     void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+                     void* workspace, size_t workspace_bytes, mla_stream_t stream,
+                     const StackedRows& stk = StackedRows{nullptr, 0u, 0u}) {
   mla_status_t st;
-  const bool chunk = buffer_row_offsets != nullptr;
+  const bool stacked = stk.T != 0;
+  const bool chunk = buffer_row_offsets != nullptr && !stacked;
   if (flags & ~MLA_CHUNK_ACCUMULATE) return fail(MLA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
   const bool contig = page_table == nullptr;
   if (!q) return fail(MLA_ERR_INVALID_ARG, "q descriptor is NULL");
@@ -1528,11 +1555,20 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   if (B < 1 || B > kMaxBatch) return fail(MLA_ERR_INVALID_ARG, "batch %lld outside 1..%u", (long long)B, kMaxBatch);
   if (P < 1 || NP < 1 || max_pages < 1) return fail(MLA_ERR_INVALID_ARG, "empty page pool or page table");
   if (NP * P > 0x7FFFFFFFll) return fail(MLA_ERR_INVALID_ARG, "page pool exceeds 2^31 slots");
-  if (chunk) {
+  if (chunk || (stacked && lse)) {
     if (!cache_offsets) return fail(MLA_ERR_INVALID_ARG, "cache_offsets is NULL");
     if ((st = check_tensor(lse, "lse", 2, MLA_DTYPE_F32)) != MLA_OK) return st;
     if (lse->shape[0] != Tq || lse->shape[1] != H) return fail(MLA_ERR_INVALID_ARG, "lse must be [Tq, H] matching q");
     if (reinterpret_cast<uintptr_t>(lse->data) & 3u) return fail(MLA_ERR_INVALID_ARG, "lse data must be 4-byte aligned");
+  }
+  if (stacked) {
+    if (!buffer_row_offsets || !cache_offsets || !stk.num_rows)
+      return fail(MLA_ERR_INVALID_ARG, "buffer_row_offsets / cache_offsets / num_rows is NULL");
+    if (stk.max_rows < 1) return fail(MLA_ERR_INVALID_ARG, "max_rows must be >= 1");
+    if (static_cast<uint64_t>(stk.max_rows) * stk.T > 0x7FFFFFFFull)
+      return fail(MLA_ERR_INVALID_ARG, "max_rows x buffer_token_size exceeds 2^31 K rows");
+    if (Sk < Tq) return fail(MLA_ERR_INVALID_ARG, "k_nope has fewer rows than q");
+  } else if (chunk) {
     if (Sk < 1) return fail(MLA_ERR_INVALID_ARG, "the buffer row holds no keys");
   } else if (Sk < Tq) {
     return fail(MLA_ERR_INVALID_ARG, "k_nope has fewer rows than q");
@@ -1646,7 +1682,7 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   prm.out = static_cast<uint16_t*>(out->data);
   prm.out_tok = out->stride[0];
   prm.out_head = out->stride[1];
-  if (chunk) {
+  if (chunk || (stacked && lse)) {
     prm.lse = static_cast<float*>(lse->data);
     prm.lse_tok = lse->stride[0];
     prm.lse_head = lse->stride[1];
@@ -1696,7 +1732,7 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     rr.out = static_cast<uint16_t*>(rope_rows);
     rr.ws = static_cast<uint8_t*>(workspace);
     return launch_attention<true, true>(prm, dev, sms, row_offsets, cache_lens, buffer_row_offsets,
-                                        cache_offsets, uB, uH, uTq, uSk, uP, uMP, workspace, &rr, cs);
+                                        cache_offsets, uB, uH, uTq, uSk, uP, uMP, workspace, &rr, stk, cs);
   }
   if (fp8) {
     const uint32_t slots = static_cast<uint32_t>(NP * P);
@@ -1709,7 +1745,7 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   }
   auto launch = fp8 ? launch_attention<true, false> : launch_attention<false, false>;
   return launch(prm, dev, sms, row_offsets, cache_lens, buffer_row_offsets, cache_offsets, uB, uH, uTq, uSk,
-                uP, uMP, workspace, nullptr, cs);
+                uP, uMP, workspace, nullptr, stk, cs);
 }
 
 }  // namespace
@@ -1775,6 +1811,19 @@ extern "C" mla_status_t mla_prefill_ragged_contiguous(const mla_tensor_t* out, c
   if (batch < 1) return mla::fail(MLA_ERR_INVALID_ARG, "batch must be >= 1");
   return mla::prefill(out, nullptr, q, nullptr, k_nope, v, k_rope, nullptr, batch, row_offsets, cache_lens,
                       nullptr, nullptr, scale, mask, 0u, workspace, workspace_bytes, stream);
+}
+
+extern "C" mla_status_t mla_prefill_ragged_chunked(
+    const mla_tensor_t* out, const mla_tensor_t* lse, const mla_tensor_t* q, const mla_tensor_t* k_nope,
+    const mla_tensor_t* v, const mla_tensor_t* k_rope_pages, const mla_tensor_t* page_table,
+    const uint32_t* row_offsets, const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
+    const uint32_t* cache_offsets, const uint32_t* num_rows, uint32_t max_rows, uint32_t buffer_token_size,
+    float scale, mla_mask_t mask, void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  if (!page_table) return mla::fail(MLA_ERR_INVALID_ARG, "page_table descriptor is NULL");
+  if (buffer_token_size < 1) return mla::fail(MLA_ERR_INVALID_ARG, "buffer_token_size must be >= 1");
+  return mla::prefill(out, lse, q, nullptr, k_nope, v, k_rope_pages, page_table, 0, row_offsets, cache_lens,
+                      buffer_row_offsets, cache_offsets, scale, mask, 0u, workspace, workspace_bytes, stream,
+                      mla::StackedRows{num_rows, max_rows, buffer_token_size});
 }
 
 extern "C" mla_status_t mla_prefill_ragged_chunk(

@@ -375,3 +375,32 @@ def test_binding_k_scale_granularity_and_workspace_rows():
     assert binding._rope_rows(k_nope, torch.ones(1), 64) == 64
     assert binding._rope_rows(k_nope, torch.ones(20), 64) == 20
     assert binding.workspace_size(3, fp8_pool_slots=20) == binding.workspace_size(3) + 20 * 128
+
+
+@pytest.mark.parametrize("case", ["no_bro", "no_co", "no_num_rows", "max_rows0", "T0", "rows_overflow",
+                                  "lse_shape", "few_k_rows"])
+def test_chunked_single_call_rejects_bad_arguments(lib, case):
+    a = _ragged_args()
+    bro, co, nrows, max_rows, T, lse = 0x50000, 0x60000, 0x70000, 3, 8, None
+    if case == "no_bro":
+        bro = None
+    elif case == "no_co":
+        co = None
+    elif case == "no_num_rows":
+        nrows = None
+    elif case == "max_rows0":
+        max_rows = 0
+    elif case == "T0":
+        T = 0
+    elif case == "rows_overflow":
+        max_rows, T = 1 << 20, 1 << 12
+    elif case == "lse_shape":
+        lse = _desc([10, 3], binding.MLA_DTYPE_F32)
+    elif case == "few_k_rows":
+        a = _ragged_args(k=_desc([5, 2, 128]), v=_desc([5, 2, 128]))
+    r = lambda d: None if d is None else ctypes.byref(d)
+    st = lib.mla_prefill_ragged_chunked(r(a["out"]), r(lse), r(a["q"]), r(a["k"]), r(a["v"]), r(a["rope"]),
+                                        r(a["pt"]), a["ro"], a["cl"], bro, co, nrows, max_rows, T, a["scale"],
+                                        a["mask"], a["ws"], a["ws_bytes"], None)
+    assert st == binding.MLA_ERR_INVALID_ARG, case
+    assert lib.mla_last_error_string()

@@ -1,6 +1,7 @@
 """Chunked execution on the GPU (mla_prefill_plan, then mla_prefill_ragged_chunk
-per buffer row, then mla_prefill_merge, all through the C ABI) versus the
-float64 oracle.
+per buffer row with mla_prefill_merge or the in-place fold, or every row in
+one mla_prefill_ragged_chunked call, all through the C ABI) versus the float64
+oracle.
 
 Per row: the row's output and lse against the oracle's window function, on
 every token of every sequence the row holds keys of (rows of the others must
@@ -163,7 +164,7 @@ def test_full_size_chunked_sampled(lib, name):
     slots = w.num_pages * w.page_size if w.spec.dtype == "fp8" else None
     ws = binding.alloc_workspace(w.batch, fp8_pool_slots=slots)
     binding.prefill_chunked(out, d["q"], d["k_nope"], d["v"], pool, d["page_table"], d["row_offsets"],
-                            d["cache_lens"], w.scale, T, S, workspace=ws, q_scale=d.get("q_scale"),
+                            d["cache_lens"], w.scale, T, -(-S // T), workspace=ws, q_scale=d.get("q_scale"),
                             k_scale=d.get("k_scale"), v_scale=d.get("v_scale"),
                             k_rope_scales=d.get("k_rope_scales"))
     assert binding.device_status(ws) == 0
@@ -176,6 +177,15 @@ def test_full_size_chunked_sampled(lib, name):
     _close(got[sel], ref[sel], oa, orr, name)
 
 
+def _case_workload(case):
+    name, kw, T = CASES[case]
+    if name is not None:
+        return workloads.generate(workloads.config(name)), T
+    kw = dict(dict(heads=2, page_size=16, seed=750 + list(CASES).index(case)), **kw)
+    n, prior = kw.pop("n"), kw.pop("prior")
+    return workloads.custom(n, prior, **kw), T
+
+
 def _full_window(w):
     from oracle import plan as oplan
     bro, co, _, R = oplan.plan_formula(w.row_offsets, w.prior, max(1, w.total_k), 1)
@@ -186,16 +196,11 @@ def _full_window(w):
 @pytest.mark.parametrize("case", ["tiny_T32", "ragged_T100_gather", "T1_one_key_rows", "page12_T37",
                                   "null_mask_T200", "long_prior_T300", "fp8_T100"])
 def test_chunked_fold_in_place(lib, case):
-    """MLA_CHUNK_ACCUMULATE: rows folded into out / lse in row order, no merge;
-    out must be the full-context result and lse the full-context lse."""
+    """MLA_CHUNK_ACCUMULATE: one mla_prefill_ragged_chunk per row, folded into
+    out / lse in row order, no merge; out must be the full-context result and
+    lse the full-context lse."""
     from mla_ragged_paged_gb300 import binding
-    name, kw, T = CASES[case]
-    if name is not None:
-        w = workloads.generate(workloads.config(name))
-    else:
-        kw = dict(dict(heads=2, page_size=16, seed=750 + list(CASES).index(case)), **kw)
-        n, prior = kw.pop("n"), kw.pop("prior")
-        w = workloads.custom(n, prior, **kw)
+    w, T = _case_workload(case)
     d = workloads.device_inputs(w)
     pool = d["k_rope_pool"][..., w.spec.rope_col:w.spec.rope_col + 64]
     slots = w.num_pages * w.page_size if w.spec.dtype == "fp8" else None
@@ -203,11 +208,17 @@ def test_chunked_fold_in_place(lib, case):
     mask = binding.MLA_MASK_CAUSAL if w.spec.mask == "causal" else binding.MLA_MASK_NULL
     out = torch.full((w.total_q, w.heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((w.total_q, w.heads), float("nan"), dtype=torch.float32, device="cuda")
-    binding.prefill_chunked(out, d["q"], d["k_nope"], d["v"], pool, d["page_table"], d["row_offsets"],
-                            d["cache_lens"], w.scale, T, w.total_k, mask=mask, workspace=ws,
-                            q_scale=d.get("q_scale"), k_scale=d.get("k_scale"), v_scale=d.get("v_scale"),
-                            k_rope_scales=d.get("k_rope_scales"), fold=True, lse=lse)
-    assert binding.device_status(ws) == 0
+    S = w.total_k
+    R = -(-S // T)
+    bro, co, _, _ = binding.plan(d["row_offsets"], d["cache_lens"], T, R)
+    for r in range(R):
+        lo, hi = r * T, min((r + 1) * T, S)
+        binding.prefill_ragged_chunk(out, lse, d["q"], d["k_nope"][lo:hi], d["v"][lo:hi], pool,
+                                     d["page_table"], d["row_offsets"], d["cache_lens"], bro[r], co[r],
+                                     w.scale, mask, ws, q_scale=d.get("q_scale"), k_scale=d.get("k_scale"),
+                                     v_scale=d.get("v_scale"), k_rope_scales=d.get("k_rope_scales"),
+                                     flags=binding.MLA_CHUNK_ACCUMULATE)
+        assert binding.device_status(ws) == 0
     got = out.float().cpu().numpy().astype(np.float64)
     got_lse = lse.cpu().numpy().astype(np.float64)
     (oa, orr), (la, lr) = _tols(w)
@@ -215,3 +226,72 @@ def test_chunked_fold_in_place(lib, case):
     _close(got, oatt.reference(w), oa, orr, f"{case} folded out")
     _, ref_lse = och.window_reference(w, *_full_window(w))
     _close(got_lse, ref_lse, la, lr, f"{case} folded lse")
+
+
+@pytest.mark.parametrize("case", list(CASES))
+@pytest.mark.parametrize("spare_rows", [0, 3])
+def test_chunked_single_call(lib, case, spare_rows):
+    """mla_prefill_ragged_chunked: the plan, then all its rows in one call over
+    the rows' K buffers stacked T rows apart; out and lse must be the
+    full-context result.  With spare plan capacity (max_rows > R) the unused
+    rows are not read."""
+    from mla_ragged_paged_gb300 import binding
+    w, T = _case_workload(case)
+    d = workloads.device_inputs(w)
+    pool = d["k_rope_pool"][..., w.spec.rope_col:w.spec.rope_col + 64]
+    slots = w.num_pages * w.page_size if w.spec.dtype == "fp8" else None
+    ws = binding.alloc_workspace(w.batch, fp8_pool_slots=slots)
+    mask = binding.MLA_MASK_CAUSAL if w.spec.mask == "causal" else binding.MLA_MASK_NULL
+    out = torch.full((w.total_q, w.heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((w.total_q, w.heads), float("nan"), dtype=torch.float32, device="cuda")
+    R = -(-w.total_k // T)
+    binding.prefill_chunked(out, d["q"], d["k_nope"], d["v"], pool, d["page_table"], d["row_offsets"],
+                            d["cache_lens"], w.scale, T, R + spare_rows, mask=mask, workspace=ws,
+                            q_scale=d.get("q_scale"), k_scale=d.get("k_scale"), v_scale=d.get("v_scale"),
+                            k_rope_scales=d.get("k_rope_scales"), lse=lse)
+    assert binding.device_status(ws) == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    got_lse = lse.cpu().numpy().astype(np.float64)
+    (oa, orr), (la, lr) = _tols(w)
+    _close(got, oatt.reference(w), oa, orr, f"{case} out")
+    _, ref_lse = och.window_reference(w, *_full_window(w))
+    _close(got_lse, ref_lse, la, lr, f"{case} lse")
+
+
+def test_chunked_single_call_checks_the_plan(lib):
+    """A plan row that disagrees with the stacked layout, or a row count that
+    leaves a sequence's last row out, skips the sequences concerned and sets
+    MLA_DEVICE_STATUS_BAD_OFFSETS; the other sequences are still correct."""
+    from mla_ragged_paged_gb300 import binding
+    w = workloads.custom([150, 40, 90], [70, 0, 30], heads=2, page_size=16, seed=790)
+    d = workloads.device_inputs(w)
+    T = 64
+    R = -(-w.total_k // T)
+    bro, co, _, nrows = binding.plan(d["row_offsets"], d["cache_lens"], T, R)
+    ws = binding.alloc_workspace(w.batch)
+    ref = oatt.reference(w)
+    q0 = [int(x) for x in w.row_offsets]
+    # Sequence 1 starts inside row 3 (G_1 = 220) at its context position 0:
+    # claim position 1 there instead.
+    bad_co = co.clone()
+    bad_co[3, 1] += 1
+    out = torch.full((w.total_q, w.heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    binding.prefill_ragged_chunked(out, d["q"], d["k_nope"], d["v"], d["k_rope_pool"], d["page_table"],
+                                   d["row_offsets"], d["cache_lens"], bro, bad_co, nrows, T, w.scale,
+                                   workspace=ws)
+    assert binding.device_status(ws) & 0x4
+    got = out.float().cpu().numpy().astype(np.float64)
+    for b in (0, 2):
+        sl = slice(q0[b], q0[b + 1])
+        _close(got[sl], ref[sl], 2e-2, 2e-2, f"sequence {b}")
+    # One row fewer than the plan needs: the last sequence's last row is missing.
+    short = torch.tensor([R - 1], dtype=torch.int32, device="cuda")
+    out.fill_(float("nan"))
+    binding.prefill_ragged_chunked(out, d["q"], d["k_nope"], d["v"], d["k_rope_pool"], d["page_table"],
+                                   d["row_offsets"], d["cache_lens"], bro, co, short, T, w.scale,
+                                   workspace=ws)
+    assert binding.device_status(ws) & 0x4
+    got = out.float().cpu().numpy().astype(np.float64)
+    for b in (0, 1):
+        sl = slice(q0[b], q0[b + 1])
+        _close(got[sl], ref[sl], 2e-2, 2e-2, f"sequence {b}")

@@ -145,17 +145,28 @@ def test_split_per_token_k(lib, case, kw, contiguous):
     _close(got, oatt.reference(w, q=q64), case)
 
 
-@pytest.mark.parametrize("fold", [False, True])
+@pytest.mark.parametrize("fold", [False, True, "single"])
 def test_chunked_per_token_k(lib, fold):
     """Plan + one chunk call per buffer row (the row's slice of the per-token
     scales with its K rows), merged or folded, against the window oracle per
-    row and the full-context oracle."""
+    row and the full-context oracle; or all rows in one
+    mla_prefill_ragged_chunked call (scales by stacked K row)."""
     from mla_ragged_paged_gb300 import binding
     w = _workload([300, 17, 513], [0, 700, 129], heads=4, page_size=16, seed=1270)
     T = 200
     d = workloads.device_inputs(w)
     S = w.total_k
     R = -(-S // T)
+    if fold == "single":
+        pool = d["k_rope_pool"][..., :64]
+        ws = binding.alloc_workspace(w.batch, fp8_pool_slots=S)
+        out = torch.full((w.total_q, w.heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        binding.prefill_chunked(out, d["q"], d["k_nope"], d["v"], pool, d["page_table"], d["row_offsets"],
+                                d["cache_lens"], w.scale, T, R, workspace=ws, q_scale=d["q_scale"],
+                                k_scale=d["k_scale"], v_scale=d["v_scale"], k_rope_scales=d["k_rope_scales"])
+        assert binding.device_status(ws) == 0
+        _close(_f64(out), oatt.reference(w), "chunked single call")
+        return
     bro, co, _, _ = binding.plan(d["row_offsets"], d["cache_lens"], T, R)
     pool = d["k_rope_pool"][..., :64]
     ws = binding.alloc_workspace(w.batch, fp8_pool_slots=max(T, w.num_pages * w.page_size))
