@@ -27,7 +27,9 @@
 //              from shared into tensor memory (tcgen05.cp), then per tile 32
 //              UMMAs M128 N128 K16 with A read from tensor memory
 //   warps 2-5  epilogue: tensor memory -> bf16 -> 128B-swizzled staging ->
-//              TMA tile store, 64 columns at a time through two 16 KB buffers
+//              TMA tile store; each warp stores its own 32 rows, 64 columns
+//              at a time through two 4 KB buffers, with no barrier between
+//              the warps
 // Tensor memory: A [0, 256), two accumulators [256, 384) and [384, 512), so
 // the epilogue of one tile overlaps the main loop of the next.  With two
 // weight matrices (K_nope and V from the same latent rows) the tiles of both
@@ -53,13 +55,13 @@ constexpr int kGStages = 6;
 constexpr int kGThreads = 192;
 constexpr uint32_t kGAtomBytes = 128 * kGAtom * 2;  // 16 KB: 128 rows of one atom
 constexpr uint32_t kGChunk = 2 * kGAtomBytes;       // a ring slot: two atoms
-constexpr uint32_t kGSlab = kGM * 64 * 2;      // 16 KB: 64 output columns of a tile
+constexpr uint32_t kGSlab = 32 * 64 * 2;       // 4 KB: 64 output columns of one warp's 32 rows
 constexpr uint32_t kGTmemCols = 512;
 constexpr uint32_t kGColAcc = kGMaxK / 2;      // accumulators after A's 256 columns
 
 struct __align__(1024) GemmSmem {
   uint8_t ring[kGStages][kGChunk];
-  uint8_t c[2][kGSlab];
+  uint8_t c[4][2][kGSlab];   // per epilogue warp, two staging buffers
   uint64_t full[kGStages], empty[kGStages];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t a_drain, drain;
@@ -71,7 +73,7 @@ static_assert(sizeof(GemmSmem) + 1024 <= 232448, "up-projection shared memory");
 struct GemmParams {
   CUtensorMap tm_a;     // contiguous A [M, K], box 64 x 128; or cache rows [slots, K], box 64 x 1
   CUtensorMap tm_b[2];  // weights [N, K], box 64 x 128
-  CUtensorMap tm_c[2];  // outputs [M, N], box 64 x 128
+  CUtensorMap tm_c[2];  // outputs [M, N], box 64 x 32
   uint32_t M, k_atoms, m_tiles, n_tiles, num_out;  // k_atoms = ceil(K / 64)
   // Row gather: buffer position t holds context token co[b] + t - bro[b] of
   // the sequence b with bro[b] <= t < bro[b+1]; its cache row (slot) is
@@ -142,6 +144,7 @@ __device__ void gemm_producer(GemmSmem& s, const GemmParams& p, int lane, volati
   uint32_t cur_m = 0xFFFFFFFFu;
   uint32_t bad = 0;
   bool alive = true;
+  const uint64_t keep = l2_policy_evict_last();
   // Claim the next ring slot and arm its barrier for `atoms` 16 KB atoms.
   auto acquire = [&](uint32_t atoms, uint32_t& bar, uint32_t& dst) -> bool {
     const uint32_t st = pos % kGStages;
@@ -182,10 +185,12 @@ __device__ void gemm_producer(GemmSmem& s, const GemmParams& p, int lane, volati
       const uint32_t na = min(2u, p.k_atoms - a0);
       uint32_t bar, dst;
       if (!(alive = acquire(na, bar, dst))) break;
+      // The weights are read once per row block: keep them in L2 against
+      // the streamed output.
       if (lane == 0)
         for (uint32_t a = 0; a < na; ++a)
-          tma_load_2d(dst + a * kGAtomBytes, &p.tm_b[ti.o], bar, static_cast<int32_t>((a0 + a) * kGAtom),
-                      static_cast<int32_t>(ti.n * kGN));
+          tma_load_2d_hint(dst + a * kGAtomBytes, &p.tm_b[ti.o], bar, static_cast<int32_t>((a0 + a) * kGAtom),
+                           static_cast<int32_t>(ti.n * kGN), keep);
     }
   }
   for (int o = 16; o; o >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o);
@@ -272,9 +277,9 @@ __device__ void gemm_epilogue(GemmSmem& s, const GemmParams& p, uint32_t tmem, i
                               volatile uint32_t* abort) {
   uint32_t t0, t1;
   tile_range(p, t0, t1);
-  const int r = quarter * 32 + lane;                     // tile row == tensor-memory lane
+  const int r = lane;                                    // row inside this warp's 32-row quarter
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-  const bool issuer = threadIdx.x == 64;                 // first epilogue thread stores
+  const uint64_t stream_out = l2_policy_evict_first();
   uint32_t tl = 0, slab = 0;
   for (uint32_t t = t0; t < t1; ++t, ++tl) {
     const TileIdx ti = tile_of(p, t);
@@ -301,9 +306,9 @@ __device__ void gemm_epilogue(GemmSmem& s, const GemmParams& p, uint32_t tmem, i
         pk[16 + e] = pack_bf16x2(__uint_as_float(v1[2 * e]), __uint_as_float(v1[2 * e + 1]));
       }
       // The store that last read this staging buffer (two slabs ago) must be done.
-      if (issuer) bulk_wait_group_read<1>();
-      named_bar_sync(1, 128);
-      const uint32_t base = smem_u32(s.c[slab & 1u]);
+      if (lane == 0) bulk_wait_group_read<1>();
+      __syncwarp();
+      const uint32_t base = smem_u32(s.c[quarter][slab & 1u]);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const uint32_t a = base + r * 128 + ((q ^ (r & 7)) << 4);
@@ -312,15 +317,16 @@ __device__ void gemm_epilogue(GemmSmem& s, const GemmParams& p, uint32_t tmem, i
                      : "memory");
       }
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (issuer) {
-        tma_store_2d(&p.tm_c[ti.o], base, static_cast<int32_t>(ti.n * kGN + c * 64),
-                     static_cast<int32_t>(ti.m * kGM));
+      __syncwarp();
+      if (lane == 0) {
+        // The output is written once and not read here: stream it through L2.
+        tma_store_2d_hint(&p.tm_c[ti.o], base, static_cast<int32_t>(ti.n * kGN + c * 64),
+                          static_cast<int32_t>(ti.m * kGM + quarter * 32), stream_out);
         bulk_commit_group();
       }
     }
   }
-  if (issuer) bulk_wait_group_all();
+  if (lane == 0) bulk_wait_group_all();
 }
 
 __global__ void __launch_bounds__(kGThreads, 1) up_project_kernel(const __grid_constant__ GemmParams p) {
@@ -409,7 +415,7 @@ mla_status_t setup_outputs(GemmParams& p, const mla_tensor_t* const* outs, const
     if (outs[o]->shape[0] != M || outs[o]->shape[1] != N)
       return fail(MLA_ERR_INVALID_ARG, "out must be [%lld, %lld]", (long long)M, (long long)N);
     if ((st = encode_matrix(&p.tm_b[o], weights[o], static_cast<uint64_t>(K), kGN, "weight")) != MLA_OK) return st;
-    if ((st = encode_matrix(&p.tm_c[o], outs[o], static_cast<uint64_t>(N), kGM, "out")) != MLA_OK) return st;
+    if ((st = encode_matrix(&p.tm_c[o], outs[o], static_cast<uint64_t>(N), 32, "out")) != MLA_OK) return st;
   }
   if (N < 1 || K < 1) return fail(MLA_ERR_INVALID_ARG, "empty projection");
   p.M = static_cast<uint32_t>(M);
