@@ -540,6 +540,24 @@ def main():
     barrier(world)
     e2e_ms = dist_max(e0.elapsed_time(e1), world)
 
+    # The host link's own rate: the same per-step input copies, pinned host ->
+    # device, one cudaMemcpyAsync per tensor on the copy stream, no compute
+    # beside them (best of three).
+    link_ms = None
+    for _ in range(3):
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s_in):
+            c0.record(s_in)
+            for k in keys:
+                sets[0][k].copy_(h[k], non_blocking=True)
+            c1.record(s_in)
+        torch.cuda.synchronize(dev)
+        t = c0.elapsed_time(c1)
+        link_ms = t if link_ms is None else min(link_ms, t)
+    link_gbs = h2d / (link_ms * 1e-3) / 1e9
+    e2e_h2d_gbs = h2d * args.e2e_steps / (e2e_ms * 1e-3) / 1e9
+
     peaks, peak_src = load_peaks()
     # fp8 UMMAs run at twice the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s dense).
     peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
@@ -615,6 +633,8 @@ def main():
             "clocks": clocks,
             "e2e": {"value": F_all * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "h2d_gbs": e2e_h2d_gbs, "link_gbs": link_gbs, "h2d_frac_of_link": e2e_h2d_gbs / link_gbs,
+                    "link_measure": "the step's input copies alone, pinned host to device, best of 3",
                     "pipelining": "two buffer sets: H2D of step i+1 and D2H of step i-1 overlap step i"},
             "gpu_launches": launches_per_step * args.steps,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,

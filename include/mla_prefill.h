@@ -187,6 +187,22 @@ mla_status_t mla_prefill_ragged(const mla_tensor_t* out, const mla_tensor_t* q,
                                 size_t workspace_bytes, mla_stream_t stream);
 
 /*
+ * mla_prefill_ragged with an optional lse output and flags
+ * (flare_mla_prefill: description; Args as mla_prefill_ragged):
+ *   lse    device float32 [Tq, H] (written) or NULL: ln sum_j exp(s_j) over
+ *          each query's visible keys (s_j the scaled scores)
+ *   flags  0 or MLA_FP8_PRECISE
+ * Everything else as mla_prefill_ragged.
+ */
+mla_status_t mla_prefill_ragged_ex(const mla_tensor_t* out, const mla_tensor_t* lse,
+                                   const mla_tensor_t* q, const mla_tensor_t* k_nope,
+                                   const mla_tensor_t* v, const mla_tensor_t* k_rope_pages,
+                                   const mla_tensor_t* page_table, const uint32_t* row_offsets,
+                                   const uint32_t* cache_lens, float scale, mla_mask_t mask,
+                                   uint32_t flags, void* workspace, size_t workspace_bytes,
+                                   mla_stream_t stream);
+
+/*
  * Ragged MLA prefill attention with a contiguous K_rope (flare_mla_prefill:
  * the overload taking k_rope as a plain tensor, and cache_offsets, which is
  * None "when the cache is contiguous").
@@ -307,7 +323,7 @@ mla_status_t mla_prefill_ragged_noalloc(const mla_tensor_t* out, const mla_tenso
  *     a sequence whose window starts at position 0 is written afresh.  After
  *     the last row, out is the full-context result and lse its log-sum-exp,
  *     with no mla_prefill_merge and no per-row buffers.  flags = 0 writes the
- *     row's own result.
+ *     row's own result.  MLA_FP8_PRECISE may be ORed in (fp8 inputs).
  *   lse          device float32 [Tq, H] (written), 4-byte aligned
  *   k_nope, v    device [S_row, H, 128] with S_row >= buffer_row_offsets[B] >= 1
  *                (fp8 per-token K_nope scales: the row's own [S_row] floats, and
@@ -328,6 +344,24 @@ mla_status_t mla_prefill_ragged_chunk(const mla_tensor_t* out, const mla_tensor_
                                       mla_stream_t stream);
 
 #define MLA_CHUNK_ACCUMULATE 0x1u /* mla_prefill_ragged_chunk*: fold into out / lse */
+/* fp8 inputs, a wider error envelope at a cost in speed: two quantities that
+ * the fp8 path rounds once are carried as two terms each, a value and the
+ * remainder of its rounding, and their products run once per term into the
+ * same accumulator: P (the softmax weights, e4m3 for the e4m3 P.V) as
+ * e4m3(P) + e4m3(P - e4m3(P)), about 7 significant bits instead of 3, and
+ * the bf16 copy of K_rope (code * s_r / s_k) as bf16 + bf16, about 16 bits
+ * instead of 8.  Measured on inputs whose values spread 1x / 2x / 3x the fp8
+ * workload's: the largest error relative to the 6e-2 + 6e-2|ref| tolerance
+ * drops from about 0.56 / 1.6 / 2.6 to 0.04 / 0.05 / 0.07.  Costs: a second
+ * e4m3 P.V pass, four more bf16 UMMAs per score tile, a third ring chunk per
+ * KV tile (the fp8 workload runs at about 0.58x the speed), and twice the
+ * workspace for the converted K_rope
+ * (mla_prefill_ragged_workspace_size_fp8 with 2 x pool_slots, or 2 x Sk with
+ * per-token K_nope scales).  Accepted by mla_prefill_ragged_ex,
+ * mla_prefill_ragged_chunked and the chunk calls; MLA_ERR_INVALID_ARG with
+ * bf16 inputs.  No counterpart on the pages, which leave the fp8 kernel's
+ * intermediate precisions open. */
+#define MLA_FP8_PRECISE 0x2u
 
 /*
  * Chunked execution of every buffer row of the plan in one call and one
@@ -355,6 +389,7 @@ mla_status_t mla_prefill_ragged_chunk(const mla_tensor_t* out, const mla_tensor_
  *         r >= min(R, max_rows) are not read
  *   k_nope, v           device [>= R * T, H, 128] (fp8 per-token K_nope
  *         scales: [rows] floats indexed by stacked K row)
+ * flags: 0 or MLA_FP8_PRECISE.
  * Per sequence the kernel checks the first and the last row holding its keys
  * against the stacked layout (offset, context position and window end); a
  * sequence whose rows disagree, or that needs a row >= min(R, max_rows), is
@@ -369,8 +404,8 @@ mla_status_t mla_prefill_ragged_chunked(const mla_tensor_t* out, const mla_tenso
                                         const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
                                         const uint32_t* cache_offsets, const uint32_t* num_rows,
                                         uint32_t max_rows, uint32_t buffer_token_size, float scale,
-                                        mla_mask_t mask, void* workspace, size_t workspace_bytes,
-                                        mla_stream_t stream);
+                                        mla_mask_t mask, uint32_t flags, void* workspace,
+                                        size_t workspace_bytes, mla_stream_t stream);
 
 /*
  * Combines the rows of a chunked execution (the pages give only the per-row

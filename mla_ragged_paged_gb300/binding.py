@@ -17,11 +17,13 @@ MLA_DTYPE_BF16, MLA_DTYPE_FP8_E4M3, MLA_DTYPE_U32, MLA_DTYPE_F32 = 0, 1, 2, 3
 MLA_MASK_CAUSAL, MLA_MASK_NULL = 0, 1
 MLA_SCALE_NONE, MLA_SCALE_PER_TENSOR, MLA_SCALE_PER_TOKEN = 0, 1, 2
 MLA_CHUNK_ACCUMULATE = 0x1
+MLA_FP8_PRECISE = 0x2
 STATUS_BITS = {0x1: "BAD_PAGE", 0x2: "BAD_COLUMN", 0x4: "BAD_OFFSETS", 0x8: "TIMEOUT"}
 
 # Names exported by the C ABI (kept in step with include/mla_prefill.h).
 EXPORTS = ["mla_prefill_plan", "mla_prefill_plan_max_rows", "mla_prefill_ragged_workspace_size",
-           "mla_prefill_ragged_workspace_size_fp8", "mla_prefill_ragged", "mla_prefill_ragged_noalloc",
+           "mla_prefill_ragged_workspace_size_fp8", "mla_prefill_ragged", "mla_prefill_ragged_ex",
+           "mla_prefill_ragged_noalloc",
            "mla_prefill_ragged_chunk", "mla_prefill_ragged_chunked", "mla_prefill_merge",
            "mla_prefill_ragged_contiguous",
            "mla_prefill_ragged_chunk_contiguous", "mla_gather_rows", "mla_up_project",
@@ -74,7 +76,10 @@ def load(path=LIB_PATH):
                                              ctypes.c_int, u32, vp, ctypes.c_size_t, vp]
     lib.mla_prefill_ragged_chunk.restype = ctypes.c_int
     lib.mla_prefill_ragged_chunked.argtypes = [pt, pt, pt, pt, pt, pt, pt, vp, vp, vp, vp, vp, u32, u32,
-                                               ctypes.c_float, ctypes.c_int, vp, ctypes.c_size_t, vp]
+                                               ctypes.c_float, ctypes.c_int, u32, vp, ctypes.c_size_t, vp]
+    lib.mla_prefill_ragged_ex.argtypes = [pt, pt, pt, pt, pt, pt, pt, vp, vp, ctypes.c_float, ctypes.c_int, u32,
+                                          vp, ctypes.c_size_t, vp]
+    lib.mla_prefill_ragged_ex.restype = ctypes.c_int
     lib.mla_prefill_ragged_chunked.restype = ctypes.c_int
     lib.mla_prefill_merge.argtypes = [pt, pt, pt, vp, vp, u32, vp]
     lib.mla_prefill_merge.restype = ctypes.c_int
@@ -240,6 +245,30 @@ def prefill_ragged(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cac
     return out
 
 
+def prefill_ragged_ex(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens, scale,
+                      mask=MLA_MASK_CAUSAL, workspace=None, lse=None, flags=0, q_scale=None, k_scale=None,
+                      v_scale=None, k_rope_scales=None, stream=None):
+    """mla_prefill_ragged_ex: mla_prefill_ragged with an optional lse [Tq, H]
+    float32 output and flags (MLA_FP8_PRECISE)."""
+    lib = load()
+    B = page_table.shape[0]
+    fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
+    if workspace is None:
+        slots = _rope_rows(k_nope, k_scale, k_rope_pages.shape[0] * k_rope_pages.shape[1]) if fp8 else None
+        if slots is not None and flags & MLA_FP8_PRECISE:
+            slots *= 2
+        workspace = alloc_workspace(B, q.device, slots)
+    d_q, d_k, d_v, d_r, d_pt = _inputs(q, k_nope, v, k_rope_pages, page_table, q_scale, k_scale,
+                                       v_scale, k_rope_scales)
+    d_out = describe(out, MLA_DTYPE_BF16)
+    d_lse = describe(lse, MLA_DTYPE_F32) if lse is not None else None
+    _check(lib.mla_prefill_ragged_ex(ctypes.byref(d_out), ctypes.byref(d_lse) if d_lse is not None else None,
+                                     ctypes.byref(d_q), ctypes.byref(d_k), ctypes.byref(d_v), ctypes.byref(d_r),
+                                     ctypes.byref(d_pt), _ptr(row_offsets), _ptr(cache_lens), float(scale),
+                                     int(mask), int(flags), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
 def _inputs(q, k_nope, v, k_rope_pages, page_table, q_scale, k_scale, v_scale, k_rope_scales):
     fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
     gran_t = MLA_SCALE_PER_TENSOR if fp8 else MLA_SCALE_NONE
@@ -264,6 +293,8 @@ def prefill_ragged_chunk(out, lse, q, k_nope, v, k_rope_pages, page_table, row_o
     fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
     if workspace is None:
         slots = _rope_rows(k_nope, k_scale, k_rope_pages.shape[0] * k_rope_pages.shape[1]) if fp8 else None
+        if slots is not None and flags & MLA_FP8_PRECISE:
+            slots *= 2
         workspace = alloc_workspace(B, q.device, slots)
     d_q, d_k, d_v, d_r, d_pt = _inputs(q, k_nope, v, k_rope_pages, page_table, q_scale, k_scale,
                                        v_scale, k_rope_scales)
@@ -452,7 +483,7 @@ def chunked_scratch(num_rows, total_q, heads, device="cuda"):
 def prefill_ragged_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offsets, cache_lens,
                            buffer_row_offsets, cache_offsets, num_rows, buffer_token_size, scale,
                            mask=MLA_MASK_CAUSAL, workspace=None, lse=None, q_scale=None, k_scale=None,
-                           v_scale=None, k_rope_scales=None, stream=None):
+                           v_scale=None, k_rope_scales=None, stream=None, flags=0):
     """mla_prefill_ragged_chunked: every buffer row of the plan in one call.
     buffer_row_offsets [max_rows, B+1] / cache_offsets [max_rows, B] / num_rows
     [1] are the plan's device outputs; k_nope / v hold the rows' K buffers
@@ -462,6 +493,8 @@ def prefill_ragged_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offs
     fp8 = _dtype_code(q) == MLA_DTYPE_FP8_E4M3
     if workspace is None:
         slots = _rope_rows(k_nope, k_scale, k_rope_pages.shape[0] * k_rope_pages.shape[1]) if fp8 else None
+        if slots is not None and flags & MLA_FP8_PRECISE:
+            slots *= 2
         workspace = alloc_workspace(B, q.device, slots)
     if buffer_row_offsets.dim() != 2 or buffer_row_offsets.shape[1] != B + 1 or \
             buffer_row_offsets.stride(0) != B + 1 or cache_offsets.dim() != 2 or \
@@ -476,8 +509,8 @@ def prefill_ragged_chunked(out, q, k_nope, v, k_rope_pages, page_table, row_offs
                                           ctypes.byref(d_r), ctypes.byref(d_pt), _ptr(row_offsets),
                                           _ptr(cache_lens), _ptr(buffer_row_offsets), _ptr(cache_offsets),
                                           _ptr(num_rows), int(buffer_row_offsets.shape[0]),
-                                          int(buffer_token_size), float(scale), int(mask), _ptr(workspace),
-                                          workspace.numel(), _stream(stream)))
+                                          int(buffer_token_size), float(scale), int(mask), int(flags),
+                                          _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
 
 

@@ -113,6 +113,7 @@ struct AttnParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_rope;
+  CUtensorMap tm_rope_lo;     // fp8 with two K_rope' terms: the remainder copy
   uint16_t* out;
   long long out_tok, out_head;
   float* lse;                 // chunked calls: [Tq, H] natural-log sum of exp(scores), else NULL
@@ -121,6 +122,7 @@ struct AttnParams {
   const uint32_t* page_table;
   long long pt_stride;
   const uint8_t* rope_base;
+  const uint8_t* rope_base_lo;  // fp8 with two K_rope' terms: the remainder copy
   long long rope_tok_bytes, rope_page_bytes;
   uint32_t max_pages, num_pages, page_size, rope_box, rope_manual;
   uint32_t rope_contig;  // K_rope row = K row (no page table)
@@ -437,9 +439,9 @@ struct GroupPos {
   uint32_t head, pad, next;  // pad == kNoPad when the group has no pad slot
 };
 constexpr uint32_t kNoPad = 0xFFFFFFFFu;
-template <bool FP8>
+template <bool FP8, bool SPLIT>
 __device__ __forceinline__ GroupPos place_k(uint32_t pos) {
-  return {pos, kNoPad, pos + (FP8 ? 2u : 3u)};
+  return {pos, kNoPad, pos + (FP8 ? (SPLIT ? 3u : 2u) : 3u)};
 }
 template <bool FP8>
 __device__ __forceinline__ GroupPos place_v(uint32_t pos) {
@@ -475,7 +477,7 @@ struct RopeFetch {
   uint32_t page, row, state;
 };
 
-template <bool FP8>
+template <bool FP8, bool SPLIT>
 __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volatile uint32_t* abort) {
   using C = Cfg<FP8>;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
@@ -525,7 +527,7 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     }
     return f;
   };
-  auto rope_gather = [&](const ItemInfo& it, int j, uint32_t ps) {
+  auto rope_gather = [&](const ItemInfo& it, int j, uint32_t ps, const uint8_t* rope_base) {
     const uint32_t dst = ring.buf(ps);
     for (int r = lane; r < kBN; r += 32) {
       const int key = j * kBN + r;
@@ -536,7 +538,7 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
       const uint32_t page = p.page_table[static_cast<long long>(it.b) * p.pt_stride + col];
       if (page >= p.num_pages) { status |= MLA_DEVICE_STATUS_BAD_PAGE; continue; }
       const uint4* src = reinterpret_cast<const uint4*>(
-          p.rope_base + page * p.rope_page_bytes +
+          rope_base + page * p.rope_page_bytes +
           static_cast<long long>(a - col * p.page_size) * p.rope_tok_bytes);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -552,19 +554,22 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
   };
   // The K group of tile j: K_nope chunks (bf16: [0:64] and [64:128] at k,
   // k+1; fp8: one 128-code chunk at k), then the bf16 K_rope chunk (for fp8
-  // inputs read from the converted copy of the pool).
+  // inputs read from the converted copy of the pool; with two K_rope' terms
+  // the remainder chunk follows it).
   auto load_k_group = [&](const ItemInfo& it, int j, uint32_t k, bool boxes, const RopeFetch& rf) -> bool {
     constexpr int kNope = FP8 ? 1 : 2;
+    constexpr int kRope = SPLIT ? 2 : 1;
     const uint32_t bar = ring.full_bar(k);
     const uint32_t kr = k + kNope;  // K_rope slot
-    for (int c = 0; c <= kNope; ++c)
+    for (int c = 0; c < kNope + kRope; ++c)
       if (!acquire(k + c)) return false;
     if (p.rope_contig) {
       // Contiguous K_rope: the tile's 128 rows sit at its K rows.
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar, (kNope + 1) * kChunk);
+        mbar_arrive_expect_tx(bar, (kNope + kRope) * kChunk);
         for (int c = 0; c < kNope; ++c) tma_chunk(&p.tm_k, 64 * c, it, j, k + c, bar);
         tma_load_2d(ring.buf(kr), &p.tm_rope, bar, 0, it.kv_row0 + j * kBN);
+        if (SPLIT) tma_load_2d(ring.buf(kr + 1), &p.tm_rope_lo, bar, 0, it.kv_row0 + j * kBN);
       }
       __syncwarp();
     } else if (boxes) {
@@ -573,17 +578,22 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
       else if (rf.state == 1 && rf.page >= p.num_pages) status |= MLA_DEVICE_STATUS_BAD_PAGE;
       else issue = rf.state == 1;
       const uint32_t mask = __ballot_sync(0xffffffffu, issue);
-      const uint32_t bytes = kNope * kChunk + __popc(mask) * p.rope_box * 128u;
+      const uint32_t bytes = kNope * kChunk + kRope * __popc(mask) * p.rope_box * 128u;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar, bytes);
         for (int c = 0; c < kNope; ++c) tma_chunk(&p.tm_k, 64 * c, it, j, k + c, bar);
       }
       __syncwarp();
-      if (issue)
+      if (issue) {
         tma_load_3d(ring.buf(kr) + lane * p.rope_box * 128u, &p.tm_rope, bar, 0,
                     static_cast<int>(rf.row), static_cast<int>(rf.page));
+        if (SPLIT)
+          tma_load_3d(ring.buf(kr + 1) + lane * p.rope_box * 128u, &p.tm_rope_lo, bar, 0,
+                      static_cast<int>(rf.row), static_cast<int>(rf.page));
+      }
     } else {
-      rope_gather(it, j, kr);
+      rope_gather(it, j, kr, p.rope_base);
+      if (SPLIT) rope_gather(it, j, kr + 1, p.rope_base_lo);
       if (lane == 0) {
         mbar_arrive_expect_tx(bar, kNope * kChunk);
         for (int c = 0; c < kNope; ++c) tma_chunk(&p.tm_k, 64 * c, it, j, k + c, bar);
@@ -643,7 +653,7 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     RopeFetch rf = {0u, 0u, 0u};
     if (boxes && nkv > 0) rf = rope_fetch(it, 0);
     auto k_group = [&](int j) -> bool {
-      const GroupPos g = place_k<FP8>(pos);
+      const GroupPos g = place_k<FP8, SPLIT>(pos);
       pos = g.next;
       if (p.test_stall && item_k == 1 && j == 0) return true;  // nothing arms this group's barrier
       const bool ok = load_k_group(it, j, g.head, boxes, rf);
@@ -764,6 +774,31 @@ __device__ void converter_warp(Smem<true>& s, const AttnParams& p, int lane, vol
   }
 }
 
+// 64 values as a bf16 row at hi and, when lo != NULL, the remainder of that
+// rounding as a second bf16 row at lo (hi + lo carries about 16 significant
+// bits).
+__device__ __forceinline__ void store_bf16_terms(const float (&f)[64], uint16_t* hi, uint16_t* lo) {
+  uint32_t w[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+  uint4* dh = reinterpret_cast<uint4*>(hi);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) dh[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  if (!lo) return;
+  uint4* dl = reinterpret_cast<uint4*>(lo);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t r[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t h = w[4 * c + e];
+      const float h0 = __uint_as_float(h << 16), h1 = __uint_as_float(h & 0xFFFF0000u);
+      r[e] = pack_bf16x2(f[8 * c + 2 * e] - h0, f[8 * c + 2 * e + 1] - h1);
+    }
+    dl[c] = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+}
+
 // fp8 inputs, once per call: K_rope' = e4m3 code * s_r[slot] / s_k in bf16 for
 // every pool slot, into the workspace ([num_pages * P] rows of 64 bf16, 128
 // bytes each).  The attention kernel then streams it like bf16 K_rope.
@@ -772,17 +807,13 @@ __global__ void __launch_bounds__(256) rope_convert_kernel(const uint8_t* __rest
                                                            uint32_t P, uint32_t slots,
                                                            const float* __restrict__ scales,
                                                            const float* __restrict__ k_scale,
-                                                           uint16_t* __restrict__ out) {
+                                                           uint16_t* __restrict__ out, uint16_t* __restrict__ out_lo) {
   const float inv_sk = 1.f / *k_scale;
   for (uint32_t sl = blockIdx.x * blockDim.x + threadIdx.x; sl < slots; sl += gridDim.x * blockDim.x) {
     const uint32_t page = sl / P, row = sl - page * P;
     float f[64];
     load_e4m3_row(pool + page * page_bytes + row * tok_bytes, scales[sl] * inv_sk, f);
-    uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(sl) * 64);
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-      dst[c] = make_uint4(pack_bf16x2(f[8 * c], f[8 * c + 1]), pack_bf16x2(f[8 * c + 2], f[8 * c + 3]),
-                          pack_bf16x2(f[8 * c + 4], f[8 * c + 5]), pack_bf16x2(f[8 * c + 6], f[8 * c + 7]));
+    store_bf16_terms(f, out + static_cast<size_t>(sl) * 64, out_lo ? out_lo + static_cast<size_t>(sl) * 64 : nullptr);
   }
 }
 
@@ -802,6 +833,7 @@ struct RopeRows {
   const float* rope_scales;       // [num_pages * P] (contiguous: [Sk])
   const float* k_scales;          // [Sk]
   uint16_t* out;                  // [Sk, 64] bf16
+  uint16_t* out_lo;               // NULL, or the remainder term [Sk, 64] bf16
   uint8_t* ws;
 };
 
@@ -825,9 +857,11 @@ __global__ void __launch_bounds__(256) rope_convert_rows_kernel(const __grid_con
         else bad |= MLA_DEVICE_STATUS_BAD_COLUMN;
         if (pg >= a.num_pages) {
           if (col < a.max_pages) bad |= MLA_DEVICE_STATUS_BAD_PAGE;
-          uint4* dst = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(row) * 64);
+          float z[64];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+          for (int c = 0; c < 64; ++c) z[c] = 0.f;
+          store_bf16_terms(z, a.out + static_cast<size_t>(row) * 64,
+                           a.out_lo ? a.out_lo + static_cast<size_t>(row) * 64 : nullptr);
           continue;
         }
         page = pg;
@@ -836,11 +870,8 @@ __global__ void __launch_bounds__(256) rope_convert_rows_kernel(const __grid_con
       const long long slot = static_cast<long long>(page) * a.P + prow;
       float f[64];
       load_e4m3_row(a.pool + page * a.page_bytes + prow * a.tok_bytes, a.rope_scales[slot] / a.k_scales[row], f);
-      uint4* dst = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(row) * 64);
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        dst[c] = make_uint4(pack_bf16x2(f[8 * c], f[8 * c + 1]), pack_bf16x2(f[8 * c + 2], f[8 * c + 3]),
-                            pack_bf16x2(f[8 * c + 4], f[8 * c + 5]), pack_bf16x2(f[8 * c + 6], f[8 * c + 7]));
+      store_bf16_terms(f, a.out + static_cast<size_t>(row) * 64,
+                       a.out_lo ? a.out_lo + static_cast<size_t>(row) * 64 : nullptr);
     }
   }
   if (bad) atomicOr(&hdr->status, bad);
@@ -855,7 +886,7 @@ __global__ void __launch_bounds__(256) rope_convert_rows_kernel(const __grid_con
 // soon as the S region is free (the softmax of the score tile before it has
 // loaded it into registers) and then P_q(j) . V(j) once P_q(j) is stored, so
 // the next score tile is computed while the softmax works on this one.
-template <bool FP8>
+template <bool FP8, bool SPLIT>
 __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t* abort) {
   using C = Cfg<FP8>;
   const auto ring = make_ring(s);
@@ -891,6 +922,12 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
       for (int k = 0; k < 4; ++k) umma_f8_ss(d_s, qd + 2 * k, kd + 2 * k, idS8, k != 0);
 #pragma unroll
       for (int k = 0; k < 4; ++k) umma_f16_ss(d_s, qd + (kChunk >> 4) + 2 * k, rd + 2 * k, idS, 1);
+      if (SPLIT) {
+        // The remainder term of K_rope' (its bf16 rounding), same Q rope atom.
+        const uint64_t rl = sw128_desc_at(ring.buf(kpos + 2));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) umma_f16_ss(d_s, qd + (kChunk >> 4) + 2 * k, rl + 2 * k, idS, 1);
+      }
     } else {
       // 3 swizzle atoms x 4 K-steps of 16.
 #pragma unroll
@@ -912,6 +949,12 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         umma_f8_ts(d_o, d_p + ks * 8, v0 + ks * (4096 >> 4), idPV8, ks ? 1u : acc0);
+      if (SPLIT) {
+        // The second e4m3 term of P (the remainder of its rounding), in the
+        // next 32 columns of the P region, into the same accumulator.
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) umma_f8_ts(d_o, d_p + 32 + ks * 8, v0 + ks * (4096 >> 4), idPV8, 1u);
+      }
     } else {
       // 8 K-steps of 16 keys, N = 128: the two V chunks sit in adjacent slots,
       // 16 KB apart (the leading byte offset between the two 64-column atoms).
@@ -934,8 +977,8 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
     tc_fence_after();
     return true;
   };
-  constexpr int kK = FP8 ? 2 : 3;  // K chunks per tile (ring order: K chunks, then V chunks)
-  constexpr int kV = C::kCPT - kK;
+  constexpr int kK = FP8 ? (SPLIT ? 3 : 2) : 3;  // K chunks per tile (ring order: K chunks, then V chunks)
+  constexpr int kV = FP8 ? 1 : 2;
 
   // Wait until the k-th S tile of query tile t has been loaded by its softmax.
   // The waits of one issuer on tile t's loads are not always consecutive: at
@@ -979,7 +1022,7 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
     // S_q(j) into the S region once the previous score tile there has been
     // loaded; a tile this query tile does not use only passes its K group back.
     auto do_s = [&](int j) -> bool {
-      const GroupPos g = place_k<FP8>(pos);
+      const GroupPos g = place_k<FP8, SPLIT>(pos);
       pos = g.next;
       if (!wait_group(g.head)) return false;
       if (j < mine) {
@@ -1033,7 +1076,7 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
   wait_drain(smem_u32(&s.drain[q]), 0);
 }
 
-template <bool FP8, bool KTOK>
+template <bool FP8, bool KTOK, bool SPLIT>
 __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, int q, int wq,
                              int lane, volatile uint32_t* abort) {
   using C = Cfg<FP8>;
@@ -1210,6 +1253,14 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
             // 4 codes per column: pairs e (even) and e+1 (odd) share one word.
             const uint32_t two = pack_e4m3x2(p0, p1);
             pk[e >> 1] = (e & 1) ? (pk[e >> 1] | (two << 16)) : two;
+            if (SPLIT) {
+              // P = e4m3(P) + e4m3(P - e4m3(P)): the rounding remainder as a
+              // second term (words 8..15 of pk), about 7 significant bits in all.
+              float h0, h1;
+              e4m3x2_to_f32(two, h0, h1);
+              const uint32_t lo = pack_e4m3x2(p0 - h0, p1 - h1);
+              pk[8 + (e >> 1)] = (e & 1) ? (pk[8 + (e >> 1)] | (lo << 16)) : lo;
+            }
           } else {
             pk[e] = pack_bf16x2(p0, p1);
           }
@@ -1225,6 +1276,11 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
 #pragma unroll
           for (int e = 0; e < 8; ++e) w8[e] = pk[e];
           tmem_st_32x32b_x8(t_p + 8 * c, w8);
+          if (SPLIT) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w8[e] = pk[8 + e];
+            tmem_st_32x32b_x8(t_p + 32 + 8 * c, w8);
+          }
         } else {
           tmem_st_32x32b_x16(t_p + 16 * c, pk);
         }
@@ -1329,7 +1385,7 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
   }
 }
 
-template <bool FP8, bool KTOK>
+template <bool FP8, bool KTOK, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<FP8>;
   extern __shared__ uint8_t smem_raw[];
@@ -1384,16 +1440,16 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const __grid
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
     if (warp == 0) {
-      producer_warp<FP8>(s, p, lane, abort);
+      producer_warp<FP8, SPLIT>(s, p, lane, abort);
     } else if (warp == 1 || warp == 2) {
-      if (lane == 0) mma_thread<FP8>(s, tmem, warp - 1, abort);
+      if (lane == 0) mma_thread<FP8, SPLIT>(s, tmem, warp - 1, abort);
       __syncwarp();
     } else if constexpr (FP8) {
       converter_warp(s, p, lane, abort);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
-    softmax_warp<FP8, KTOK>(s, p, tmem, (warp - 4) >> 2, warp & 3, lane, abort);
+    softmax_warp<FP8, KTOK, SPLIT>(s, p, tmem, (warp - 4) >> 2, warp & 3, lane, abort);
   }
 
   tc_fence_before();
@@ -1424,14 +1480,14 @@ namespace {
 
 // Launches the scheduler, the per-row K_rope conversion (per-token K scales
 // only, rows != NULL) and the attention kernel for one input type.
-template <bool FP8, bool KTOK>
+template <bool FP8, bool KTOK, bool SPLIT>
 mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t* row_offsets,
                               const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
                               const uint32_t* cache_offsets, uint32_t B, uint32_t H, uint32_t Tq,
                               uint32_t Sk, uint32_t P, uint32_t max_pages, void* workspace,
                               const RopeRows* rows, const StackedRows& stk, cudaStream_t cs) {
   mla_status_t st;
-  auto* kernel = mla_attention_kernel<FP8, KTOK>;
+  auto* kernel = mla_attention_kernel<FP8, KTOK, SPLIT>;
   {
     // The register split inside the kernel is only safe when the kernel was
     // built with exactly kLaunchRegs registers per thread.
@@ -1452,7 +1508,7 @@ mla_status_t launch_attention(AttnParams& prm, int dev, int sms, const uint32_t*
   const int attn_smem = static_cast<int>(sizeof(Smem<FP8>) + 1024);
   // One attribute cache slot per kernel instantiation.
   if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), attn_smem, dev,
-                                 FP8 ? (KTOK ? 4 : 3) : 2)) != MLA_OK)
+                                 FP8 ? (SPLIT ? (KTOK ? 7 : 6) : (KTOK ? 4 : 3)) : 2)) != MLA_OK)
     return st;
   const uint32_t elt = FP8 ? 1u : 2u;
   schedule_kernel<<<1, kSchedThreads, sched_smem, cs>>>(row_offsets, cache_lens, buffer_row_offsets,
@@ -1492,11 +1548,15 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   mla_status_t st;
   const bool stacked = stk.T != 0;
   const bool chunk = buffer_row_offsets != nullptr && !stacked;
-  if (flags & ~MLA_CHUNK_ACCUMULATE) return fail(MLA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if (flags & ~(MLA_CHUNK_ACCUMULATE | MLA_FP8_PRECISE)) return fail(MLA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if ((flags & MLA_CHUNK_ACCUMULATE) && buffer_row_offsets == nullptr)
+    return fail(MLA_ERR_INVALID_ARG, "MLA_CHUNK_ACCUMULATE applies to the per-row chunk calls only");
+  const bool fp8_precise = (flags & MLA_FP8_PRECISE) != 0;
   const bool contig = page_table == nullptr;
   if (!q) return fail(MLA_ERR_INVALID_ARG, "q descriptor is NULL");
   const bool fp8 = q->dtype == MLA_DTYPE_FP8_E4M3;
   const mla_dtype_t dt = fp8 ? MLA_DTYPE_FP8_E4M3 : MLA_DTYPE_BF16;
+  if (fp8_precise && !fp8) return fail(MLA_ERR_INVALID_ARG, "MLA_FP8_PRECISE needs fp8 inputs");
   if ((st = check_tensor(q, "q", 3, dt)) != MLA_OK) return st;
   if ((st = check_tensor(out, "out", 3, MLA_DTYPE_BF16)) != MLA_OK) return st;
   if ((st = check_tensor(k_nope, "k_nope", 3, dt)) != MLA_OK) return st;
@@ -1555,8 +1615,8 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   if (B < 1 || B > kMaxBatch) return fail(MLA_ERR_INVALID_ARG, "batch %lld outside 1..%u", (long long)B, kMaxBatch);
   if (P < 1 || NP < 1 || max_pages < 1) return fail(MLA_ERR_INVALID_ARG, "empty page pool or page table");
   if (NP * P > 0x7FFFFFFFll) return fail(MLA_ERR_INVALID_ARG, "page pool exceeds 2^31 slots");
-  if (chunk || (stacked && lse)) {
-    if (!cache_offsets) return fail(MLA_ERR_INVALID_ARG, "cache_offsets is NULL");
+  if (chunk || lse) {
+    if (chunk && !cache_offsets) return fail(MLA_ERR_INVALID_ARG, "cache_offsets is NULL");
     if ((st = check_tensor(lse, "lse", 2, MLA_DTYPE_F32)) != MLA_OK) return st;
     if (lse->shape[0] != Tq || lse->shape[1] != H) return fail(MLA_ERR_INVALID_ARG, "lse must be [Tq, H] matching q");
     if (reinterpret_cast<uintptr_t>(lse->data) & 3u) return fail(MLA_ERR_INVALID_ARG, "lse data must be 4-byte aligned");
@@ -1579,8 +1639,10 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     return fail(MLA_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
   // fp8: the bf16 K_rope' copy has one row per pool slot, or per K row when
   // K scales are per token.
-  const size_t ws_need = fp8 ? mla_prefill_ragged_workspace_size_fp8(
-                                   static_cast<uint32_t>(B), static_cast<uint64_t>(ktok ? Sk : NP * P))
+  // With two K_rope' terms the remainder copy follows the first.
+  const uint64_t rope_slots = static_cast<uint64_t>(ktok ? Sk : NP * P);
+  const size_t ws_need = fp8 ? mla_prefill_ragged_workspace_size_fp8(static_cast<uint32_t>(B),
+                                                                     rope_slots * (fp8_precise ? 2u : 1u))
                              : mla_prefill_ragged_workspace_size(static_cast<uint32_t>(B));
   if (workspace_bytes < ws_need)
     return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes needed", ws_need);
@@ -1658,10 +1720,12 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   void* rope_rows = k_rope_pages->data;
   uint64_t rope_tok = static_cast<uint64_t>(rope_tok_el) * 2;
   uint64_t rope_page = static_cast<uint64_t>(k_rope_pages->stride[0]) * 2;
+  void* rope_rows_lo = nullptr;
   if (fp8) {
     rope_rows = static_cast<uint8_t*>(workspace) + mla_prefill_ragged_workspace_size(static_cast<uint32_t>(B));
     rope_tok = 128;
     rope_page = static_cast<uint64_t>(P) * 128;
+    if (fp8_precise) rope_rows_lo = static_cast<uint8_t*>(rope_rows) + rope_slots * 128;
   }
   if (rows_contig) {
     // One 128-row box per KV tile, at the tile's K row.
@@ -1671,6 +1735,9 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     if ((st = encode_tiled(&prm.tm_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rope_rows, dims, str, box,
                            CU_TENSOR_MAP_SWIZZLE_128B, "k_rope")) != MLA_OK)
       return st;
+    if (rope_rows_lo && (st = encode_tiled(&prm.tm_rope_lo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rope_rows_lo, dims,
+                                           str, box, CU_TENSOR_MAP_SWIZZLE_128B, "k_rope remainder")) != MLA_OK)
+      return st;
   } else if (!prm.rope_manual) {
     uint64_t dims[3] = {64, (uint64_t)P, (uint64_t)NP};
     uint64_t str[2] = {rope_tok, rope_page};
@@ -1678,11 +1745,14 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     if ((st = encode_tiled(&prm.tm_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rope_rows, dims, str, box,
                            CU_TENSOR_MAP_SWIZZLE_128B, "k_rope_pages")) != MLA_OK)
       return st;
+    if (rope_rows_lo && (st = encode_tiled(&prm.tm_rope_lo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rope_rows_lo, dims,
+                                           str, box, CU_TENSOR_MAP_SWIZZLE_128B, "k_rope remainder")) != MLA_OK)
+      return st;
   }
   prm.out = static_cast<uint16_t*>(out->data);
   prm.out_tok = out->stride[0];
   prm.out_head = out->stride[1];
-  if (chunk || (stacked && lse)) {
+  if (chunk || lse) {
     prm.lse = static_cast<float*>(lse->data);
     prm.lse_tok = lse->stride[0];
     prm.lse_head = lse->stride[1];
@@ -1691,6 +1761,7 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   prm.page_table = contig ? nullptr : static_cast<const uint32_t*>(page_table->data);
   prm.pt_stride = contig ? 0 : page_table->stride[0];
   prm.rope_base = static_cast<const uint8_t*>(rope_rows);
+  prm.rope_base_lo = static_cast<const uint8_t*>(rope_rows_lo);
   prm.rope_tok_bytes = static_cast<long long>(rope_tok);
   prm.rope_page_bytes = static_cast<long long>(rope_page);
   prm.max_pages = static_cast<uint32_t>(max_pages);
@@ -1730,8 +1801,10 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     rr.rope_scales = k_rope_pages->scale;
     rr.k_scales = k_nope->scale;
     rr.out = static_cast<uint16_t*>(rope_rows);
+    rr.out_lo = static_cast<uint16_t*>(rope_rows_lo);
     rr.ws = static_cast<uint8_t*>(workspace);
-    return launch_attention<true, true>(prm, dev, sms, row_offsets, cache_lens, buffer_row_offsets,
+    auto launch_k = fp8_precise ? launch_attention<true, true, true> : launch_attention<true, true, false>;
+    return launch_k(prm, dev, sms, row_offsets, cache_lens, buffer_row_offsets,
                                         cache_offsets, uB, uH, uTq, uSk, uP, uMP, workspace, &rr, stk, cs);
   }
   if (fp8) {
@@ -1739,11 +1812,13 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
     const int blocks = static_cast<int>(std::min<uint32_t>((slots + 255) / 256, 16u * sms));
     rope_convert_kernel<<<blocks, 256, 0, cs>>>(
         static_cast<const uint8_t*>(k_rope_pages->data), rope_tok_el, k_rope_pages->stride[0],
-        static_cast<uint32_t>(P), slots, k_rope_pages->scale, k_nope->scale, static_cast<uint16_t*>(rope_rows));
+        static_cast<uint32_t>(P), slots, k_rope_pages->scale, k_nope->scale, static_cast<uint16_t*>(rope_rows),
+        static_cast<uint16_t*>(rope_rows_lo));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "rope conversion launch: %s", cudaGetErrorString(e));
   }
-  auto launch = fp8 ? launch_attention<true, false> : launch_attention<false, false>;
+  auto launch = !fp8 ? launch_attention<false, false, false>
+                     : fp8_precise ? launch_attention<true, false, true> : launch_attention<true, false, false>;
   return launch(prm, dev, sms, row_offsets, cache_lens, buffer_row_offsets, cache_offsets, uB, uH, uTq, uSk,
                 uP, uMP, workspace, nullptr, stk, cs);
 }
@@ -1818,12 +1893,27 @@ extern "C" mla_status_t mla_prefill_ragged_chunked(
     const mla_tensor_t* v, const mla_tensor_t* k_rope_pages, const mla_tensor_t* page_table,
     const uint32_t* row_offsets, const uint32_t* cache_lens, const uint32_t* buffer_row_offsets,
     const uint32_t* cache_offsets, const uint32_t* num_rows, uint32_t max_rows, uint32_t buffer_token_size,
-    float scale, mla_mask_t mask, void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+    float scale, mla_mask_t mask, uint32_t flags, void* workspace, size_t workspace_bytes,
+    mla_stream_t stream) {
   if (!page_table) return mla::fail(MLA_ERR_INVALID_ARG, "page_table descriptor is NULL");
   if (buffer_token_size < 1) return mla::fail(MLA_ERR_INVALID_ARG, "buffer_token_size must be >= 1");
+  if (flags & MLA_CHUNK_ACCUMULATE)
+    return mla::fail(MLA_ERR_INVALID_ARG, "MLA_CHUNK_ACCUMULATE applies to the per-row chunk calls only");
   return mla::prefill(out, lse, q, nullptr, k_nope, v, k_rope_pages, page_table, 0, row_offsets, cache_lens,
-                      buffer_row_offsets, cache_offsets, scale, mask, 0u, workspace, workspace_bytes, stream,
+                      buffer_row_offsets, cache_offsets, scale, mask, flags, workspace, workspace_bytes, stream,
                       mla::StackedRows{num_rows, max_rows, buffer_token_size});
+}
+
+extern "C" mla_status_t mla_prefill_ragged_ex(const mla_tensor_t* out, const mla_tensor_t* lse,
+                                              const mla_tensor_t* q, const mla_tensor_t* k_nope,
+                                              const mla_tensor_t* v, const mla_tensor_t* k_rope_pages,
+                                              const mla_tensor_t* page_table, const uint32_t* row_offsets,
+                                              const uint32_t* cache_lens, float scale, mla_mask_t mask,
+                                              uint32_t flags, void* workspace, size_t workspace_bytes,
+                                              mla_stream_t stream) {
+  if (!page_table) return mla::fail(MLA_ERR_INVALID_ARG, "page_table descriptor is NULL");
+  return mla::prefill(out, lse, q, nullptr, k_nope, v, k_rope_pages, page_table, 0, row_offsets, cache_lens,
+                      nullptr, nullptr, scale, mask, flags, workspace, workspace_bytes, stream);
 }
 
 extern "C" mla_status_t mla_prefill_ragged_chunk(

@@ -352,6 +352,14 @@ __device__ __forceinline__ void e4m3x4_to_f32(uint32_t v, float& f0, float& f1, 
       : "=f"(f2), "=f"(f3)
       : "r"(hi));
 }
+// Two e4m3 codes (byte 0 first) -> two floats (exact).
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t v, float& f0, float& f1) {
+  uint32_t h;
+  asm("{\n .reg .b16 a;\n cvt.u16.u32 a, %1;\n cvt.rn.f16x2.e4m3x2 %0, a;\n}\n" : "=r"(h) : "r"(v));
+  asm("{\n .reg .f16 h0, h1;\n mov.b32 {h0, h1}, %2;\n cvt.f32.f16 %0, h0;\n cvt.f32.f16 %1, h1;\n}\n"
+      : "=f"(f0), "=f"(f1)
+      : "r"(h));
+}
 // Two floats -> two e4m3 codes (round to nearest even, saturating), lo in byte 0.
 __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
   uint16_t r;

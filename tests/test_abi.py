@@ -378,10 +378,10 @@ def test_binding_k_scale_granularity_and_workspace_rows():
 
 
 @pytest.mark.parametrize("case", ["no_bro", "no_co", "no_num_rows", "max_rows0", "T0", "rows_overflow",
-                                  "lse_shape", "few_k_rows"])
+                                  "lse_shape", "few_k_rows", "accumulate", "split_bf16", "unknown_flag"])
 def test_chunked_single_call_rejects_bad_arguments(lib, case):
     a = _ragged_args()
-    bro, co, nrows, max_rows, T, lse = 0x50000, 0x60000, 0x70000, 3, 8, None
+    bro, co, nrows, max_rows, T, lse, flags = 0x50000, 0x60000, 0x70000, 3, 8, None, 0
     if case == "no_bro":
         bro = None
     elif case == "no_co":
@@ -398,9 +398,34 @@ def test_chunked_single_call_rejects_bad_arguments(lib, case):
         lse = _desc([10, 3], binding.MLA_DTYPE_F32)
     elif case == "few_k_rows":
         a = _ragged_args(k=_desc([5, 2, 128]), v=_desc([5, 2, 128]))
+    elif case == "accumulate":
+        flags = binding.MLA_CHUNK_ACCUMULATE
+    elif case == "split_bf16":
+        flags = binding.MLA_FP8_PRECISE
+    elif case == "unknown_flag":
+        flags = 0x80
     r = lambda d: None if d is None else ctypes.byref(d)
     st = lib.mla_prefill_ragged_chunked(r(a["out"]), r(lse), r(a["q"]), r(a["k"]), r(a["v"]), r(a["rope"]),
                                         r(a["pt"]), a["ro"], a["cl"], bro, co, nrows, max_rows, T, a["scale"],
-                                        a["mask"], a["ws"], a["ws_bytes"], None)
+                                        a["mask"], flags, a["ws"], a["ws_bytes"], None)
+    assert st == binding.MLA_ERR_INVALID_ARG, case
+    assert lib.mla_last_error_string()
+
+
+@pytest.mark.parametrize("case", ["split_bf16", "accumulate", "unknown_flag", "lse_shape"])
+def test_ragged_ex_rejects_bad_arguments(lib, case):
+    a = _ragged_args()
+    lse, flags = None, 0
+    if case == "split_bf16":
+        flags = binding.MLA_FP8_PRECISE
+    elif case == "accumulate":
+        flags = binding.MLA_CHUNK_ACCUMULATE
+    elif case == "unknown_flag":
+        flags = 0x40
+    elif case == "lse_shape":
+        lse = _desc([10, 3], binding.MLA_DTYPE_F32)
+    r = lambda d: None if d is None else ctypes.byref(d)
+    st = lib.mla_prefill_ragged_ex(r(a["out"]), r(lse), r(a["q"]), r(a["k"]), r(a["v"]), r(a["rope"]), r(a["pt"]),
+                                   a["ro"], a["cl"], a["scale"], a["mask"], flags, a["ws"], a["ws_bytes"], None)
     assert st == binding.MLA_ERR_INVALID_ARG, case
     assert lib.mla_last_error_string()
