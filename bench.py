@@ -50,8 +50,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic of one attention launch per workload, from the ncu captures
 # summarised in profiles/; valid only while the kernel source is unchanged.
-ATTENTION_TRAFFIC = {"source_sha1": "3ced0e5c2fdcc8831802c7e84e3f2b5ce673ad08",
-                     "bytes_per_launch": {"deepseek_v3_bf16": 2395125248, "fp8_e4m3": 3183165440}}
+ATTENTION_TRAFFIC = {"source_sha1": "f4342ebfa0cb8ee40fa6a93090827514938ae784",
+                     "bytes_per_launch": {"deepseek_v3_bf16": 2394930688, "fp8_e4m3": 3182452480}}
 
 
 def causal_flops(w):

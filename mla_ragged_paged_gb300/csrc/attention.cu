@@ -8,8 +8,9 @@
 //   P_q  = exp2(S_q * scale * log2(e) - m)   (one thread per query row)
 //   O_q += P_q . V                           (UMMA, A = P read from TMEM)
 // The two Q tiles ping-pong so one tile's softmax overlaps the other tile's
-// GEMMs, and a tile's next S is computed while its softmax runs.  K_rope (64 dims shared by every head) is fetched from the paged
-// pool through the page table.
+// GEMMs, and a tile's next S is computed while its softmax runs.  K_rope (64
+// dims shared by every head) is fetched from the paged pool through the page
+// table.
 //
 // Warp roles (384 threads = three warpgroups, one warp of each per SM
 // sub-partition):
@@ -38,6 +39,15 @@
 // V (e4m3, MN-major).  S = s_q s_k (q_nope . k_nope [e4m3 UMMA] + q_rope .
 // k_rope' [bf16 UMMA]) accumulates both parts in one fp32 tile; P is
 // quantised to e4m3 after a 2^6 prescale and P.V runs as an e4m3 UMMA.
+// With MLA_FP8_PRECISE (template flag SPLIT) P and K_rope' are each carried
+// as a value plus the remainder of its rounding: P's remainder in the next
+// 32 columns of its region with a second e4m3 P.V pass, K_rope''s in a third
+// ring chunk per KV tile with four more bf16 UMMAs.
+//
+// Entry points: the full-context call (one window per sequence, its whole
+// context), one buffer row of chunked execution (the row's window per
+// sequence, optional in-place fold), and all buffer rows at once over their
+// stacked K buffers (one window per sequence spanning its rows).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
