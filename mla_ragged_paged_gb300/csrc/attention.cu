@@ -923,7 +923,11 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
     tc_fence_after();
     return true;
   };
-  // S_q = Q_q . [K_nope | K_rope]^T.
+  // S_q = Q_q . [K_nope | K_rope]^T.  bf16: each K chunk's empty barrier is
+  // committed right after the UMMAs that read it, so the producer can refill
+  // a slot while the rest of the score tile is still being computed (the
+  // eight-slot bf16 ring is short of room for the copies in flight; the fp8
+  // ring is not, and there the extra commits cost more than they return).
   auto issue_s = [&](uint32_t kpos) {
     if (FP8) {
       // 4 e4m3 K-steps of 32 over the nope atom, then 4 bf16 K-steps of 16 over rope.
@@ -946,6 +950,7 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           umma_f16_ss(d_s, qd + a * (kChunk >> 4) + 2 * k, kd + 2 * k, idS, (a | k) != 0);
+        umma_commit(ring.empty_bar(kpos + a));
       }
     }
     umma_commit(smem_u32(&s.s_full[q]));
@@ -1045,10 +1050,12 @@ __device__ void mma_thread(Smem<FP8>& s, uint32_t tmem, int q, volatile uint32_t
         uint32_t k;
         pred(j, t, k);
         if (!wait_region(t, k)) return false;
-        issue_s(g.head);
+        issue_s(g.head);  // bf16: releases the group's chunks
         if (j + 1 == mine) umma_commit(smem_u32(&s.q_empty[q]));  // Q_q no longer read
+        if (FP8) release(g.head, kK);
+      } else {
+        release(g.head, kK);
       }
-      release(g.head, kK);
       return true;
     };
     // O_q (+)= P_q(j) . V(j) once the softmax has stored P_q(j).
@@ -1098,7 +1105,9 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
   // fp8: S in TMEM is in units of s_q * s_k (per-token K scales: s_q * s_k[key],
   // the key's factor applied per column below); P, O and the row sum l carry
   // the kPScale prescale (folded into the exponent), so O / l needs only s_v.
-  const float sl2 = FP8 ? p.sl2 * (*p.q_scale) * (KTOK ? 1.f : *p.k_scale) : p.sl2;
+  // Clamped away from 0 (a zero scale) so that a masked -inf score stays -inf
+  // after the scaling FMA; any real scale is far above the clamp.
+  const float sl2 = fmaxf(FP8 ? p.sl2 * (*p.q_scale) * (KTOK ? 1.f : *p.k_scale) : p.sl2, 1e-30f);
   const float out_scale = FP8 ? *p.v_scale : 1.f;
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
   uint32_t item_k = 0, sf = 0, of = 0;
@@ -1244,7 +1253,6 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int col = 32 * c + 2 * e;
           float x0, x1;
           if (KTOK) {
             x0 = __uint_as_float(sr[c][2 * e]);
@@ -1253,11 +1261,8 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1])),
                              sl2x2, negm), x0, x1);
           }
-          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          if (masked) {
-            p0 = col < nvalid ? p0 : 0.f;
-            p1 = col + 1 < nvalid ? p1 : 0.f;
-          }
+          // A masked score is -inf here (sl2 > 0), so its exponential is 0.
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           lacc = f2_add(lacc, f2_pack(p0, p1));
           if (FP8) {
             // 4 codes per column: pairs e (even) and e+1 (odd) share one word.
