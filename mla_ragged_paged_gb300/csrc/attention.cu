@@ -1215,11 +1215,27 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
             if (32 * c + e >= nvalid) sr[c][e] = __float_as_uint(-INFINITY);
       }
       float smax = -INFINITY;
+      if (KTOK) {
+        // Eight independent chains, then a short tree (the 3-input max does
+        // not reassociate); measured faster here, neutral elsewhere.
+        float mx[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+        for (int k = 0; k < 8; ++k) {
+          const int c = k >> 1, e0 = (k & 1) * 16;
+          mx[k] = max3(__uint_as_float(sr[c][e0]), __uint_as_float(sr[c][e0 + 1]), __uint_as_float(sr[c][e0 + 2]));
 #pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          smax = max3(smax, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+          for (int e = 3; e < 15; e += 2)
+            mx[k] = max3(mx[k], __uint_as_float(sr[c][e0 + e]), __uint_as_float(sr[c][e0 + e + 1]));
+          mx[k] = fmaxf(mx[k], __uint_as_float(sr[c][e0 + 15]));
+        }
+        smax = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            smax = max3(smax, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+      }
       const float m_tile = smax == -INFINITY ? -INFINITY
                            : KTOK           ? smax - C::kPScaleLog2 + mb
                                             : smax * sl2;
@@ -1305,21 +1321,23 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
       l += l0 + l1;
       ++pvc;
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // The previous P.V of this tile has completed (see the P stores).
+        // The previous P.V of this tile has completed (see the P stores).  The
+        // score registers are free again: the whole O row goes through them
+        // in one load, one wait and one store.
         const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t o[16];
-          tmem_ld_32x32b_x16(t_o + 16 * c, o);
-          tmem_ld_wait();
+        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(t_o + 32 * c, sr[c]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
             float x0, x1;
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), x0, x1);
-            o[e] = __float_as_uint(x0);
-            o[e + 1] = __float_as_uint(x1);
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), a2), x0, x1);
+            sr[c][e] = __float_as_uint(x0);
+            sr[c][e + 1] = __float_as_uint(x1);
           }
-          tmem_st_32x32b_x16(t_o + 16 * c, o);
+          tmem_st_32x32b_x32(t_o + 32 * c, sr[c]);
         }
       }
       tmem_st_wait();
