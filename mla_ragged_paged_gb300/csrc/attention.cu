@@ -681,9 +681,13 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
       return load_v_group(it, j, g.head);
     };
     if (nkv > 0) {
-      alive = k_group(0);
-      // A query tile that sees no key of the window is not loaded.
-      if (alive) alive = (it.nkv0 == 0 || load_q(0, it)) && (it.nkv1 == 0 || load_q(1, it));
+      // Q first: its buffers free up as soon as the previous item's last
+      // score tiles are issued, while the K group's ring slots come free only
+      // after that item's last P.V; issued after K, the Q copy's latency would
+      // fall between the items.  A query tile that sees no key of the window
+      // is not loaded.
+      alive = (it.nkv0 == 0 || load_q(0, it)) && (it.nkv1 == 0 || load_q(1, it));
+      if (alive) alive = k_group(0);
     }
     for (int j = 0; j < nkv && alive; ++j) {
       if (j + 1 < nkv) alive = k_group(j + 1);
