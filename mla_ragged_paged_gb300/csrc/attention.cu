@@ -642,10 +642,15 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
     return true;
   };
 
+  // The next item is claimed two KV tiles before the end of the current one,
+  // so the counter's round trip overlaps the last loads; lane 0 holds the
+  // claimed index until the item starts.
+  uint32_t t_claim = 0;
+  bool claimed = false;
   while (alive) {
-    uint32_t t = 0;
-    if (lane == 0) t = atomicAdd(&hdr->counter, 1u);
-    t = __shfl_sync(0xffffffffu, t, 0);
+    if (!claimed && lane == 0) t_claim = atomicAdd(&hdr->counter, 1u);
+    claimed = false;
+    const uint32_t t = __shfl_sync(0xffffffffu, t_claim, 0);
     const ItemInfo it = decode_item(t, hdr, recs, p.H, p.causal);
     const uint32_t islot = item_k & 1u;
     if (!mbar_wait(smem_u32(&s.item_empty[islot]), ((item_k >> 1) & 1u) ^ 1u, abort)) break;
@@ -690,6 +695,10 @@ __device__ void producer_warp(Smem<FP8>& s, const AttnParams& p, int lane, volat
       if (alive) alive = k_group(0);
     }
     for (int j = 0; j < nkv && alive; ++j) {
+      if (j + 2 == nkv) {
+        if (lane == 0) t_claim = atomicAdd(&hdr->counter, 1u);
+        claimed = true;
+      }
       if (j + 1 < nkv) alive = k_group(j + 1);
       alive = alive && v_group(j);
     }
