@@ -126,6 +126,7 @@ struct AttnParams {
   CUtensorMap tm_rope_lo;     // fp8 with two K_rope' terms: the remainder copy
   uint16_t* out;
   long long out_tok, out_head;
+  uint32_t out_v8;            // out rows start 32-byte aligned: the epilogue uses 32-byte stores
   float* lse;                 // chunked calls: [Tq, H] natural-log sum of exp(scores), else NULL
   long long lse_tok, lse_head;
   uint32_t accumulate;        // chunked calls: fold into out / lse of the earlier rows
@@ -1420,9 +1421,15 @@ __device__ void softmax_warp(Smem<FP8>& s, const AttnParams& p, uint32_t tmem, i
         }
       }
       if (store) {
+        if (p.out_v8) {
+          // 32-byte stores: whole sectors, half the store instructions.
+          st_global_v8(dst + 4 * c, pk);
+          st_global_v8(dst + 4 * c + 2, pk + 8);
+        } else {
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-          dst[4 * c + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int v = 0; v < 4; ++v)
+            dst[4 * c + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
       }
     }
     tc_fence_before();
@@ -1798,6 +1805,10 @@ mla_status_t prefill(const mla_tensor_t* out, const mla_tensor_t* lse, const mla
   prm.out = static_cast<uint16_t*>(out->data);
   prm.out_tok = out->stride[0];
   prm.out_head = out->stride[1];
+  prm.out_v8 = (reinterpret_cast<uintptr_t>(out->data) % 32u == 0 && (prm.out_tok * 2) % 32 == 0 &&
+                (prm.out_head * 2) % 32 == 0)
+                   ? 1u
+                   : 0u;
   if (chunk || lse) {
     prm.lse = static_cast<float*>(lse->data);
     prm.lse_tok = lse->stride[0];

@@ -191,3 +191,26 @@ def test_largest_batches(lib, B, dtype):
     got, status = run_gpu(w)
     assert status == 0
     assert_close(got, oatt.reference(w), f"B={B}", *tol(w))
+
+
+@pytest.mark.parametrize("offset", [0, 8, 16])
+def test_output_alignment(lib, offset):
+    """Output rows 32-byte aligned (offset 0 or 16 bf16) take the kernel's
+    32-byte store path, rows only 16-byte aligned (offset 8) the 16-byte one;
+    both must write exactly the output rows, within tolerance of the oracle."""
+    from mla_ragged_paged_gb300 import binding
+    w = workloads.custom([200, 37, 129], [0, 50, 300], heads=3, page_size=32, seed=611)
+    d = workloads.device_inputs(w)
+    # Each (token, head) row sits at `offset` inside a 144-element slot: the row
+    # strides (144 and 3 * 144 elements) are 32-byte multiples, so only the
+    # base offset decides the alignment.
+    buf = torch.full((w.total_q * w.heads * 144 + 16,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = buf[offset:offset + w.total_q * w.heads * 144].view(w.total_q, w.heads, 144)[..., :128]
+    ws = binding.alloc_workspace(w.batch)
+    binding.prefill_ragged(out, d["q"], d["k_nope"], d["v"], d["k_rope_pool"], d["page_table"],
+                           d["row_offsets"], d["cache_lens"], w.scale, binding.MLA_MASK_CAUSAL, ws)
+    assert binding.device_status(ws) == 0
+    torch.cuda.synchronize()
+    slots = buf[offset:offset + w.total_q * w.heads * 144].view(w.total_q, w.heads, 144)
+    assert torch.isnan(slots[..., 128:]).all(), "the kernel wrote outside the output rows"
+    assert_close(out.float().cpu().numpy().astype(np.float64), oatt.reference(w), f"offset {offset}")
