@@ -50,8 +50,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic of one attention launch per workload, from the ncu captures
 # summarised in profiles/; valid only while the kernel source is unchanged.
-ATTENTION_TRAFFIC = {"source_sha1": "9f331585bb4883cb63b5921304967a308606a5d6",
-                     "bytes_per_launch": {"deepseek_v3_bf16": 2396639488, "fp8_e4m3": 3185156608}}
+ATTENTION_TRAFFIC = {"source_sha1": "a4fea7fad2f013099c92a0be7b2506f181e00ea7",
+                     "bytes_per_launch": {"deepseek_v3_bf16": 2401581568, "fp8_e4m3": 3197671424}}
 
 
 def causal_flops(w):

@@ -354,7 +354,7 @@ mla_status_t mla_prefill_ragged_chunk(const mla_tensor_t* out, const mla_tensor_
  * workload's: the largest error relative to the 6e-2 + 6e-2|ref| tolerance
  * drops from about 0.56 / 1.6 / 2.6 to 0.04 / 0.05 / 0.07.  Costs: a second
  * e4m3 P.V pass, four more bf16 UMMAs per score tile, a third ring chunk per
- * KV tile (the fp8 workload runs at about 0.58x the speed), and twice the
+ * KV tile (the fp8 workload runs at about 0.59x the speed), and twice the
  * workspace for the converted K_rope
  * (mla_prefill_ragged_workspace_size_fp8 with 2 x pool_slots, or 2 x Sk with
  * per-token K_nope scales).  Accepted by mla_prefill_ragged_ex,
